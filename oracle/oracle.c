@@ -1,0 +1,349 @@
+/*
+ * CSA2 CPU oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU restatement of what one CSA2 attention
+ * layer of DeepSeek-V4.1-Flash computes at decode and chunked prefill.  It is
+ * used only by the test suite, by the smoke check and by the CPU-baseline leg of
+ * the benchmark; the product library never links or calls it.  It shares no
+ * code, header, table or constant generator with the CUDA path.
+ *
+ * Sources (page title, section):
+ *   [P1] "DeepSeek's Attention and KV Cache - From MLA to CSA2, From First
+ *        Principles": "A Precision Primer" (E4M3, E2M1, block scaling),
+ *        "DeepSeek-V3.2: Sparse Attention With a Learned Indexer" (index score,
+ *        top-k), "DeepSeek-V4" (window concatenated with the selected entries,
+ *        shared-KV MQA), "DeepSeek-V4.1 ... Four bits for the main KV" (E2M1
+ *        with one E4M3 scale per 16 channels, no global scale, 288 B entry,
+ *        numpy quantizer check).
+ *   [P2] "From MLA to DSA to HCA/CSA: DeepSeek V3.2 and V4 Attention":
+ *        "The indexer" (ReLU score, head sum, fp32 scoring path),
+ *        "CSA: two changes to HCA" (-1 sentinel when fewer than k are
+ *        visible), "What replaced MLA" (K and V are the same tensor).
+ *   [P3] "DeepSeek-V4.1-Flash and the 890-byte KV cache", section 3
+ *        (indexer key in the main-KV format: 72 B per entry).
+ *
+ * Precision: codecs decide integer codes in fp32 (the kernel's precision);
+ * every dot product, score, softmax and output accumulation is fp64.
+ *
+ * Cache layout (the pages give entry sizes only; the layout is this build's
+ * reading and is restated here from its definition, independently of the GPU
+ * code):
+ *   page = 128 entries.  Page id of (request r, page j) is bt[r*max_pages+j],
+ *   or r*max_pages+j when bt == NULL.
+ *   main-KV page: 128 * 288 B.  Entry e at e*288: bytes [0,256) hold channel
+ *     pairs (2i, 2i+1) as low/high nibble of byte i; bytes [256,288) hold the
+ *     32 block scales in block order.
+ *   indexer-K page: 9216 B = 128 * 72 B.  Nibbles of entry e, channel c at
+ *     (e/8)*512 + (c/32)*128 + (e%8)*16 + (c%32)/2 (low nibble = even c);
+ *     scale of entry e, block b at 8192 + (b/4)*512 + (e%32)*16 + (e/32)*4 + b%4.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_D 512
+#define OR_DI 128
+#define OR_PAGE 128
+#define OR_KV_BYTES 288
+#define OR_IDX_BYTES 72
+#define OR_KV_PAGE_BYTES (OR_PAGE * OR_KV_BYTES)
+#define OR_IDX_PAGE_BYTES (OR_PAGE * OR_IDX_BYTES)
+
+/* ---------------------------------------------------------------- bf16 */
+
+static float bf16_to_float(uint16_t h) {
+  uint32_t u = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* ------------------------------------------------------------ E4M3 [P1]
+ * E4M3 (FN variant): 1 sign, 4 exponent bits with bias 7, 3 mantissa bits.
+ * Exponent field 0 is subnormal (m * 2^-9); the all-ones pattern 0x7F/0xFF is
+ * the single NaN; there is no infinity; the largest finite value is 448.
+ */
+double or_e4m3_decode(uint8_t c) {
+  int s = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* Round-to-nearest-even onto the E4M3 grid, saturating to +-448 (satfinite).
+ * x is an fp32 value; all arithmetic below is exact in double. */
+uint8_t or_e4m3_encode(float xf) {
+  double x = (double)xf;
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  if (isnan(x)) return 0x7F;
+  if (a >= 448.0) return sign | 0x7E; /* satfinite */
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: a = q * 2^-9, q in [0, 8) */
+    double q = ldexp(a, 9);
+    double fl = floor(q), fr = q - fl;
+    int qi = (int)fl;
+    if (fr > 0.5 || (fr == 0.5 && (qi & 1))) qi += 1;
+    /* qi == 8 becomes the smallest normal: field (e=1, m=0) = 0x08 */
+    return sign | (uint8_t)qi;
+  }
+  int e2;
+  double fr = frexp(a, &e2); /* a = fr * 2^e2, fr in [0.5, 1) */
+  int e = e2 - 1;            /* a = (2*fr) * 2^e, 2*fr in [1, 2) */
+  double mant = (2.0 * fr - 1.0) * 8.0; /* in [0, 8) */
+  double fl = floor(mant), rem = mant - fl;
+  int mi = (int)fl;
+  if (rem > 0.5 || (rem == 0.5 && (mi & 1))) mi += 1;
+  if (mi == 8) { mi = 0; e += 1; }
+  int field = e + 7;
+  /* a < 448 so the rounded value is at most 448 = (field 15, m 6) */
+  return sign | (uint8_t)((field << 3) | mi);
+}
+
+/* ------------------------------------------------------------ E2M1 [P1]
+ * E2M1: 1 sign, 2 exponent bits, 1 mantissa bit.  Magnitudes of codes 0..7 are
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 is the sign; no infinity, no NaN.
+ */
+static const double e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double or_e2m1_decode(uint8_t c) {
+  double v = e2m1_mag[c & 7];
+  return (c & 8) ? -v : v;
+}
+
+/* Nearest magnitude, ties to the even code (mantissa bit 0), |y| > 6 -> 6.
+ * The sign bit is kept even when the magnitude rounds to 0. */
+uint8_t or_e2m1_encode(float yf) {
+  double y = (double)yf;
+  uint8_t sign = signbit(y) ? 8 : 0;
+  double a = fabs(y);
+  if (a >= 6.0) return sign | 7;
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    double dc = fabs(a - e2m1_mag[c]), db = fabs(a - e2m1_mag[best]);
+    if (dc < db || (dc == db && (c & 1) == 0 && (best & 1) == 1)) best = c;
+  }
+  return sign | (uint8_t)best;
+}
+
+/* ---------------------------------------------------- block of 16 [P1]
+ * One E4M3 scale per 16 channels mapping the block maximum onto 6; the
+ * second-level tensor scale of NVFP4 is omitted.  amax/6 and x/s are
+ * correctly rounded fp32 divisions; a zero scale encodes the block as +0. */
+void or_quant_block16(const float* x, uint8_t* codes, uint8_t* scale_code) {
+  float amax = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  volatile float ratio = amax / 6.0f; /* fp32 division */
+  uint8_t sc = or_e4m3_encode(ratio);
+  *scale_code = sc;
+  float s = (float)or_e4m3_decode(sc);
+  for (int i = 0; i < 16; ++i) {
+    if (s == 0.0f) {
+      codes[i] = 0;
+    } else {
+      volatile float y = x[i] / s; /* fp32 division */
+      codes[i] = or_e2m1_encode(y);
+    }
+  }
+}
+
+/* ---------------------------------------------------------- cache layout */
+
+static int64_t page_of(const int32_t* bt, int32_t max_pages, int32_t r, int64_t s) {
+  int64_t j = s / OR_PAGE;
+  return bt ? (int64_t)bt[(int64_t)r * max_pages + j] : (int64_t)r * max_pages + j;
+}
+
+static int64_t idx_nib_off(int64_t e, int64_t c) {
+  return (e / 8) * 512 + (c / 32) * 128 + (e % 8) * 16 + (c % 32) / 2;
+}
+
+static int64_t idx_sf_off(int64_t e, int64_t b) {
+  return 8192 + (b / 4) * 512 + (e % 32) * 16 + (e / 32) * 4 + (b % 4);
+}
+
+/* Write one 512-channel main-KV entry and one 128-channel indexer-K entry. */
+static void write_entry(const float* lat, const float* key, uint8_t* kv_pages, uint8_t* idx_pages,
+                        int64_t page, int64_t e) {
+  uint8_t* rec = kv_pages + page * OR_KV_PAGE_BYTES + e * OR_KV_BYTES;
+  for (int b = 0; b < 32; ++b) {
+    uint8_t codes[16], sc;
+    or_quant_block16(lat + 16 * b, codes, &sc);
+    for (int i = 0; i < 8; ++i) rec[b * 8 + i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));
+    rec[256 + b] = sc;
+  }
+  uint8_t* pg = idx_pages + page * OR_IDX_PAGE_BYTES;
+  for (int b = 0; b < 8; ++b) {
+    uint8_t codes[16], sc;
+    or_quant_block16(key + 16 * b, codes, &sc);
+    for (int i = 0; i < 16; i += 2) {
+      int64_t c = 16 * b + i;
+      pg[idx_nib_off(e, c)] = (uint8_t)(codes[i] | (codes[i + 1] << 4));
+    }
+    pg[idx_sf_off(e, b)] = sc;
+  }
+}
+
+/* Pack n new entries (bf16 latents [n][512], bf16 indexer keys [n][128]) at
+ * positions pos[i] of requests req[i]. */
+void or_pack_kv(const uint16_t* latent, const uint16_t* idx_key, const int32_t* req,
+                const int64_t* pos, int64_t n, uint8_t* kv_pages, uint8_t* idx_pages,
+                const int32_t* bt, int32_t max_pages) {
+  float lat[OR_D], key[OR_DI];
+  for (int64_t i = 0; i < n; ++i) {
+    for (int c = 0; c < OR_D; ++c) lat[c] = bf16_to_float(latent[i * OR_D + c]);
+    for (int c = 0; c < OR_DI; ++c) key[c] = bf16_to_float(idx_key[i * OR_DI + c]);
+    int64_t page = page_of(bt, max_pages, req[i], pos[i]);
+    write_entry(lat, key, kv_pages, idx_pages, page, pos[i] % OR_PAGE);
+  }
+}
+
+/* Pack fp32 vectors (used by the quantizer check on an fp32 latent). */
+void or_quant_vector(const float* x, int64_t nblocks, uint8_t* codes, uint8_t* scales) {
+  for (int64_t b = 0; b < nblocks; ++b) or_quant_block16(x + 16 * b, codes + 16 * b, scales + b);
+}
+
+/* Dequantised values of one cached entry: v = e2m1(code) * e4m3(scale). */
+void or_read_main(const uint8_t* kv_pages, const int32_t* bt, int32_t max_pages, int32_t r,
+                  int64_t s, double* out) {
+  const uint8_t* rec = kv_pages + page_of(bt, max_pages, r, s) * OR_KV_PAGE_BYTES +
+                       (s % OR_PAGE) * OR_KV_BYTES;
+  for (int c = 0; c < OR_D; ++c) {
+    uint8_t byte = rec[c / 2];
+    uint8_t code = (c % 2) ? (byte >> 4) : (byte & 15);
+    out[c] = or_e2m1_decode(code) * or_e4m3_decode(rec[256 + c / 16]);
+  }
+}
+
+void or_read_idx(const uint8_t* idx_pages, const int32_t* bt, int32_t max_pages, int32_t r,
+                 int64_t s, double* out) {
+  const uint8_t* pg = idx_pages + page_of(bt, max_pages, r, s) * OR_IDX_PAGE_BYTES;
+  int64_t e = s % OR_PAGE;
+  for (int c = 0; c < OR_DI; ++c) {
+    uint8_t byte = pg[idx_nib_off(e, c)];
+    uint8_t code = (c % 2) ? (byte >> 4) : (byte & 15);
+    out[c] = or_e2m1_decode(code) * or_e4m3_decode(pg[idx_sf_off(e, c / 16)]);
+  }
+}
+
+/* ----------------------------------------------------- index score [P1][P2]
+ * I[t,s] = sum_j w[t,j] * ReLU( qhat[t,j] . khat[s] * 128^-0.5 ), for
+ * s in [s0, s1).  qhat is the indexer query quantised with the same block
+ * codec (the query-key product is taken entirely in FP4).  M[t,s] is the same
+ * sum with |w| (the scale for the score tolerance).  All in fp64. */
+void or_index_score(const uint16_t* q_idx, const float* w, int32_t heads, const uint8_t* idx_pages,
+                    const int32_t* bt, int32_t max_pages, int32_t r, int64_t s0, int64_t s1,
+                    double* I, double* M) {
+  double* qh = (double*)malloc(sizeof(double) * heads * OR_DI);
+  for (int j = 0; j < heads; ++j) {
+    for (int b = 0; b < 8; ++b) {
+      float x[16];
+      uint8_t codes[16], sc;
+      for (int i = 0; i < 16; ++i) x[i] = bf16_to_float(q_idx[(int64_t)j * OR_DI + 16 * b + i]);
+      or_quant_block16(x, codes, &sc);
+      for (int i = 0; i < 16; ++i)
+        qh[j * OR_DI + 16 * b + i] = or_e2m1_decode(codes[i]) * or_e4m3_decode(sc);
+    }
+  }
+  const double scale = 1.0 / sqrt(128.0);
+  double k[OR_DI];
+  for (int64_t s = s0; s < s1; ++s) {
+    or_read_idx(idx_pages, bt, max_pages, r, s, k);
+    double acc = 0.0, accm = 0.0;
+    for (int j = 0; j < heads; ++j) {
+      double dot = 0.0;
+      for (int c = 0; c < OR_DI; ++c) dot += qh[j * OR_DI + c] * k[c];
+      double relu = dot * scale > 0.0 ? dot * scale : 0.0;
+      acc += (double)w[j] * relu;
+      accm += fabs((double)w[j]) * relu;
+    }
+    I[s - s0] = acc;
+    M[s - s0] = accm;
+  }
+  free(qh);
+}
+
+/* --------------------------------------------------------------- top-k [P2]
+ * The k largest scores among the n visible entries; equal scores are ordered
+ * by the lower index first; -0 and +0 are equal.  The chosen indices are
+ * returned in ascending order, padded with -1 when n < k. */
+typedef struct { float v; int64_t i; } or_pair;
+
+static int cmp_pair(const void* a, const void* b) {
+  const or_pair* x = (const or_pair*)a;
+  const or_pair* y = (const or_pair*)b;
+  if (x->v > y->v) return -1;
+  if (x->v < y->v) return 1;
+  return (x->i < y->i) ? -1 : (x->i > y->i);
+}
+
+static int cmp_i32(const void* a, const void* b) {
+  int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return (x > y) - (x < y);
+}
+
+void or_topk(const float* scores, int64_t n, int32_t k, int32_t* out) {
+  or_pair* p = (or_pair*)malloc(sizeof(or_pair) * (n > 0 ? n : 1));
+  for (int64_t i = 0; i < n; ++i) {
+    float v = scores[i];
+    p[i].v = (v == 0.0f) ? 0.0f : v; /* -0 -> +0 */
+    p[i].i = i;
+  }
+  qsort(p, (size_t)n, sizeof(or_pair), cmp_pair);
+  int64_t take = n < k ? n : k;
+  for (int64_t i = 0; i < take; ++i) out[i] = (int32_t)p[i].i;
+  qsort(out, (size_t)take, sizeof(int32_t), cmp_i32);
+  for (int64_t i = take; i < k; ++i) out[i] = -1;
+  free(p);
+}
+
+/* ------------------------------------------------ sparse + window MQA [P1][P2]
+ * Keys = the dequantised entries named by idx (entries < 0 are skipped) followed
+ * by the win_len bf16 window rows; no de-duplication.  Each key is both key and
+ * value.  For each head h: S = scale * q_h . key, P = softmax(S), O_h = P . keys,
+ * lse_h = log(sum exp S).  Two passes, fp64.  With no keys, O = 0, lse = -inf. */
+void or_attention(const uint16_t* q, int32_t heads, const int32_t* idx, int32_t k,
+                  const uint8_t* kv_pages, const int32_t* bt, int32_t max_pages, int32_t r,
+                  const uint16_t* win, int32_t win_len, double scale, double* O, double* lse) {
+  int32_t nk = 0;
+  for (int i = 0; i < k; ++i) nk += idx[i] >= 0;
+  nk += win_len;
+  double* keys = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1) * OR_D);
+  int32_t t = 0;
+  for (int i = 0; i < k; ++i)
+    if (idx[i] >= 0) or_read_main(kv_pages, bt, max_pages, r, idx[i], keys + (int64_t)(t++) * OR_D);
+  for (int i = 0; i < win_len; ++i, ++t)
+    for (int c = 0; c < OR_D; ++c) keys[(int64_t)t * OR_D + c] = bf16_to_float(win[(int64_t)i * OR_D + c]);
+  double* S = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1));
+  double qd[OR_D];
+  for (int h = 0; h < heads; ++h) {
+    for (int c = 0; c < OR_D; ++c) qd[c] = bf16_to_float(q[(int64_t)h * OR_D + c]);
+    double* o = O + (int64_t)h * OR_D;
+    for (int c = 0; c < OR_D; ++c) o[c] = 0.0;
+    if (nk == 0) { lse[h] = -INFINITY; continue; }
+    double mx = -INFINITY;
+    for (int j = 0; j < nk; ++j) {
+      double dot = 0.0;
+      for (int c = 0; c < OR_D; ++c) dot += qd[c] * keys[(int64_t)j * OR_D + c];
+      S[j] = scale * dot;
+      if (S[j] > mx) mx = S[j];
+    }
+    double sum = 0.0;
+    for (int j = 0; j < nk; ++j) { S[j] = exp(S[j] - mx); sum += S[j]; }
+    for (int j = 0; j < nk; ++j) {
+      double p = S[j] / sum;
+      for (int c = 0; c < OR_D; ++c) o[c] += p * keys[(int64_t)j * OR_D + c];
+    }
+    lse[h] = mx + log(sum);
+  }
+  free(S);
+  free(keys);
+}
