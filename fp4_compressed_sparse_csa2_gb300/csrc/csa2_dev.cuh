@@ -1,0 +1,319 @@
+// csa2_dev.cuh -- device helpers shared by the CSA2 kernels (sm_103a only).
+//
+// Inline-PTX wrappers for the Blackwell tensor-core path (tcgen05 MMA, TMEM,
+// tcgen05.cp), bulk async copies with mbarrier completion, bounded waits, the
+// E2M1/E4M3 block codec and the cache-page layouts.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+// ----------------------------------------------------------------- error word
+// Workspace header: ws[0] = first error status, ws[1] = info code.
+enum ErrInfo : int32_t {
+  kInfoPage = 1,      // page id outside [0, n_pages)
+  kInfoPos = 2,       // position beyond the request's pages
+  kInfoTopkIdx = 3,   // a selected index outside [0, n_visible)
+  kInfoGroup = 4,     // queries of one indexer group belong to different requests
+  kInfoWait = 5,      // a bounded pipeline wait ran out
+};
+
+__device__ __forceinline__ void report(int32_t* err, int32_t status, int32_t info) {
+  if (err != nullptr && atomicCAS(err, 0, status) == 0) atomicExch(err + 1, info);
+}
+
+// Bound for every spin wait: about 2 s of wall time (globaltimer, ns).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ----------------------------------------------------------------- smem / mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and never blocks longer than
+// kWaitLimitNs) when the phase did not complete or *abort became non-zero.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Generic-proxy shared-memory writes become visible to the async proxy (tensor core).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- TMEM / tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {  // whole warp
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, no swizzle ("interleaved" core matrices of
+// 8 rows x 16 bytes).  lbo: byte stride between core matrices along K (K-major) /
+// along K (MN-major); sbo: byte stride between core matrices along M/N.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
+  return d;                             // base offset 0, swizzle none
+}
+
+// Instruction descriptor, kind::f16 with bf16 operands and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+         (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf4nvf4: E2M1 x E2M1, UE4M3 scale per 16 elements.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (0u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], "
+      "p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once all previously issued tcgen05 operations of this thread finish.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Copy a 32-row x 16-byte scale-factor atom from shared memory to TMEM, replicated
+// into the four 32-lane quarters.
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc_src) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc_src) : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ----------------------------------------------------------------- codec
+// E4M3 (bias 7, subnormals, max 448) and E2M1 (magnitudes 0,.5,1,1.5,2,3,4,6) with
+// round-to-nearest-even and saturation, through the hardware conversions.
+__device__ __forceinline__ uint32_t cvt_e4m3(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return r & 0xFFu;  // second source lands in the low byte
+}
+
+// Two values -> one byte: `lo` in bits 0-3, `hi` in bits 4-7.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  const float v = e ? ldexpf(1.0f + 0.125f * static_cast<float>(m), static_cast<int>(e) - 7)
+                    : ldexpf(static_cast<float>(m), -9);
+  return (c & 0x80u) ? -v : v;
+}
+
+// Quantise 16 fp32 values: returns the scale code; writes 8 bytes of nibbles
+// (value 2i in the low nibble of byte i).
+__device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], uint32_t& nib_lo, uint32_t& nib_hi) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const uint32_t sc = cvt_e4m3(__fdiv_rn(amax, 6.0f));
+  const float s = e4m3_value(sc);
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (s == 0.0f)
+      b[i] = 0u;
+    else
+      b[i] = cvt_e2m1x2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s));
+  }
+  nib_lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+  nib_hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+  return sc;
+}
+
+// 8 packed E2M1 codes (one 32-bit word: code 2i low nibble / 2i+1 high nibble of
+// byte i) times a bf16x2 scale -> 4 bf16x2 words, exactly (a product has at most 6
+// significant bits and lies in [2^-10, 2688]).  Byte lookups with PRMT: the low and
+// high bytes of the bf16 pattern of each magnitude, the sign from the code's bit 3.
+__device__ __forceinline__ void dequant8_bf16(uint32_t w, __nv_bfloat162 scale2, uint32_t (&out)[4]) {
+  // bf16 of magnitudes 0,.5,1,1.5,2,3,4,6: high bytes 00,3F,3F,3F,40,40,40,40;
+  // low bytes 00,00,80,C0,00,40,80,C0.
+  const uint32_t kHiA = 0x3F3F3F00u, kHiB = 0x40404040u;
+  const uint32_t kLoA = 0xC0800000u, kLoB = 0xC0804000u;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t c = (w >> (16 * half)) & 0xFFFFu;  // 4 codes e0..e3 in nibbles
+    const uint32_t sel = c & 0x7777u;
+    uint32_t lo, hi, sg;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(kLoA), "r"(kLoB), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(kHiA), "r"(kHiB), "r"(sel));
+    // sign bytes: replicate the msb of bytes holding each code's sign bit
+    asm("prmt.b32 %0, %1, %2, 0xD9C8;" : "=r"(sg) : "r"(c << 4), "r"(c));
+    hi |= sg & 0x80808080u;
+    uint32_t w0, w1;
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(w0) : "r"(lo), "r"(hi));
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(w1) : "r"(lo), "r"(hi));
+    __nv_bfloat162 v0 = *reinterpret_cast<__nv_bfloat162*>(&w0);
+    __nv_bfloat162 v1 = *reinterpret_cast<__nv_bfloat162*>(&w1);
+    v0 = __hmul2(v0, scale2);
+    v1 = __hmul2(v1, scale2);
+    out[2 * half] = *reinterpret_cast<uint32_t*>(&v0);
+    out[2 * half + 1] = *reinterpret_cast<uint32_t*>(&v1);
+  }
+}
+
+// ----------------------------------------------------------------- cache layout
+constexpr int kD = CSA2_D, kDI = CSA2_DI, kPage = CSA2_PAGE;
+constexpr int kKvBytes = CSA2_KV_BYTES, kKvPageBytes = CSA2_KV_PAGE_BYTES;
+constexpr int kIdxPageBytes = CSA2_IDX_PAGE_BYTES;
+constexpr int kIdxNibBytes = 8192;  // nibble region of an indexer page
+
+__device__ __forceinline__ int64_t page_id(const csa2_cache& c, int32_t r, int64_t s) {
+  const int64_t j = s / kPage;
+  return c.block_table ? static_cast<int64_t>(c.block_table[static_cast<int64_t>(r) * c.max_pages + j])
+                       : static_cast<int64_t>(r) * c.max_pages + j;
+}
+
+// Indexer operand layout (also used for the packed indexer query): row n, channel
+// block b (16 channels) -> 8-byte slot of its nibbles, and its scale byte.
+__device__ __forceinline__ uint32_t idx_nib_off(uint32_t n, uint32_t b) {
+  return (n >> 3) * 512u + (b >> 1) * 128u + (n & 7u) * 16u + (b & 1u) * 8u;
+}
+__device__ __forceinline__ uint32_t idx_sf_off(uint32_t nib_bytes, uint32_t n, uint32_t b) {
+  return nib_bytes + (b >> 2) * 512u + (n & 31u) * 16u + (n >> 5) * 4u + (b & 3u);
+}
+
+}  // namespace csa2

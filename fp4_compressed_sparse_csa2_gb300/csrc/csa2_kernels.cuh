@@ -1,0 +1,92 @@
+// csa2_kernels.cuh -- argument blocks and launchers of the CSA2 kernels.
+#pragma once
+
+#include "csa2_dev.cuh"
+
+namespace csa2 {
+
+struct PackArgs {
+  // new cache entries
+  const __nv_bfloat16* latent;   // [n_new][512]
+  const __nv_bfloat16* idx_key;  // [n_new][128]
+  const int32_t* new_req;
+  const int64_t* new_pos;
+  int64_t n_new;
+  csa2_cache cache;
+  // indexer query groups
+  const __nv_bfloat16* q_idx;  // [n_q][heads_I][128]
+  int64_t n_q;
+  int32_t heads_I;
+  int32_t G;           // queries per group
+  int32_t N;           // G * heads_I rows per group (<= 128)
+  int32_t grp_bytes;   // N*64 + 1024
+  int64_t n_groups;
+  uint8_t* qpack;      // [n_groups][grp_bytes]
+  int32_t* err;
+};
+
+struct IndexArgs {
+  const uint8_t* idx_pages;
+  csa2_cache cache;
+  const uint8_t* qpack;
+  int32_t grp_bytes;
+  const float* w;
+  const int32_t* req;
+  const int32_t* n_visible;
+  float* scores;
+  int64_t ld;
+  int64_t n_q;
+  int32_t heads_I;
+  int32_t G;
+  int32_t N;
+  int64_t n_groups;
+  int32_t tpg;     // tiles (pages) per group
+  int32_t stages;  // smem ring depth
+  uint32_t tmem_cols;
+  int32_t* err;
+};
+
+struct TopkArgs {
+  const float* scores;
+  int64_t ld;
+  const int32_t* n_visible;
+  int64_t n_q;
+  int32_t k;
+  int32_t* out;
+  uint32_t* hist;  // [n_q][kBins]
+  uint32_t* cnt;   // [n_q][2]  selection count, candidate count
+  int32_t* sel;    // [n_q][k]
+  uint2* cand;     // [n_q][kCandCap]  (key, index)
+  int64_t t_max;
+  int32_t* err;
+};
+
+struct AttnArgs {
+  const __nv_bfloat16* q;  // [n_q][64][512]
+  const int32_t* topk_idx; // [n_q][512]
+  const int32_t* n_visible;
+  const int32_t* req;
+  const __nv_bfloat16* window;
+  const int64_t* win_start;
+  const int32_t* win_len;
+  csa2_cache cache;
+  float scale_log2;  // softmax scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;
+  int64_t n_q;
+  int32_t* err;
+};
+
+using TraceFn = void (*)(int, cudaStream_t);
+
+cudaError_t launch_pack(const PackArgs& a, cudaStream_t stream);
+size_t index_smem_bytes(int stages);
+cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream);
+size_t topk_ws_bytes(int64_t n_q);
+void topk_carve(uint8_t* base, int64_t n_q, TopkArgs& a);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream, int kind_hist, int kind_sel, int kind_final,
+                        TraceFn trace_begin, TraceFn trace_end);
+size_t attn_smem_bytes();
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace csa2

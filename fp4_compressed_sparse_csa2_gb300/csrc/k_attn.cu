@@ -1,0 +1,364 @@
+// k_attn.cu -- shared-KV MQA over the selected FP4 entries plus the sliding window.
+//
+// "DeepSeek's Attention and KV Cache - From MLA to CSA2", "DeepSeek-V4": a query
+// attends to the top-512 selected entries concatenated with the 128 window entries;
+// each entry is one 512-wide vector serving as both key and value.  "DeepSeek-V4.1":
+// the FP4 entries are dequantised before attention.  "From MLA to DSA to HCA/CSA",
+// "What replaced MLA": attention(q, kv, kv) with K and V the same tensor.
+//
+// Design (one CTA of 8 warps per query; 64 heads; 5 key tiles of 128 keys):
+//   build    all warps gather 128 entries (16-byte loads of the 288-byte records),
+//            dequantise in registers (byte-permute lookups, exact bf16 products) and
+//            store the bf16 tile in the tensor-core operand layout; window rows are
+//            copied with cp.async;
+//   S^T      one thread issues 32 tcgen05.mma kind::f16 (M = 128 keys, N = 64 heads,
+//            K = 512) into TMEM;
+//   softmax  thread = key, 32 heads per thread: warp max reductions, a per-head
+//            reference max that only moves when a tile exceeds it by 2^8 (then the
+//            TMEM accumulator and the running sums are rescaled), exp2, bf16 P^T to
+//            shared memory;
+//   O^T      32 tcgen05.mma (4 M-tiles of 128 output channels, N = 64 heads, K = 128
+//            keys) reading the SAME bf16 tile as an MN-major operand (K == V);
+//   epilogue O = O^T / l per head -> bf16, lse = ln(sum exp).
+#include "csa2_kernels.cuh"
+
+namespace csa2 {
+
+constexpr int kAttnThreads = 256;
+constexpr int kHeads = 64;
+constexpr uint32_t kKtBytes = 128 * 512 * 2;   // bf16 key tile
+constexpr uint32_t kQsBytes = 64 * 512 * 2;    // bf16 queries
+constexpr uint32_t kPsBytes = 128 * 64 * 2;    // bf16 P^T
+constexpr uint32_t kOCols = 0, kSCols = 256;   // TMEM columns
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
+
+// Offset of element (row, col) in a [rows][512] bf16 operand tile stored as 8x8 core
+// matrices: row groups of 8 at 8192-byte stride, 8-column chunks at 128-byte stride.
+__device__ __forceinline__ uint32_t tile_off(uint32_t row, uint32_t col) {
+  return (row >> 3) * 8192u + (col >> 3) * 128u + (row & 7u) * 16u + (col & 7u) * 2u;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t sdst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sdst), "l"(gsrc), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(e4m3_value(code));
+  return __nv_bfloat162(b, b);
+}
+
+// Key validity of entry `slot` of tile `t` (t < 4: selected, t == 4: window).
+__device__ __forceinline__ bool key_valid(const AttnArgs& a, int64_t qi, int t, int slot, int32_t nv, int32_t wl,
+                                          int64_t* page_out, int32_t* e_out) {
+  if (t == 4) return slot < wl;
+  const int32_t e = __ldg(a.topk_idx + qi * CSA2_TOPK + t * 128 + slot);
+  if (e < 0) return false;
+  if (e >= nv) return false;
+  const int32_t r = __ldg(a.req + qi);
+  const int64_t p = page_id(a.cache, r, e);
+  if (p < 0 || p >= a.cache.n_pages) return false;
+  *page_out = p;
+  *e_out = e;
+  return true;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Kt = smem;
+  uint8_t* Qs = Kt + kKtBytes;
+  uint8_t* Ps = Qs + kQsBytes;
+  float* ref = reinterpret_cast<float*>(Ps + kPsBytes);  // [64] reference max (log2 units)
+  float* alpha = ref + kHeads;                            // [64]
+  float* tmax = alpha + kHeads;                           // [4][64]
+  float* lred = tmax + 4 * kHeads;                        // [4][64]
+  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(lred + 4 * kHeads);
+  uint64_t* drain = mma_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int32_t* flags = reinterpret_cast<int32_t*>(tmem_slot + 1);  // [0] abort, [1] rescale, [2] count
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t qi = blockIdx.x;
+  const int32_t nv = __ldg(a.n_visible + qi);
+  const int32_t wl = max(0, min(CSA2_WIN, __ldg(a.win_len + qi)));
+
+  if (tid == 0) {
+    mbar_init(mma_bar, 1);
+    mbar_init(drain, 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (tid < kHeads) ref[tid] = -INFINITY;
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  // queries -> shared memory (operand layout, K-major over the 512 channels)
+  {
+    const __nv_bfloat16* qg = a.q + qi * kHeads * CSA2_D;
+    for (int c = tid; c < kHeads * 64; c += kAttnThreads) {
+      const uint32_t h = c >> 6, ch = c & 63;
+      cp_async16(smem_u32(Qs + tile_off(h, ch * 8)), qg + h * CSA2_D + ch * 8, 16);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
+  const uint32_t idesc_o = idesc_bf16(128, 64, 1, 1);
+
+  float lsum[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) lsum[i] = 0.0f;
+  uint32_t phase = 0;
+  bool o_started = false;
+  const int hb = (warp >> 2) * 32;                 // this thread's 32 heads
+  const uint32_t key_row = (warp & 3) * 32 + lane; // TMEM lane = key (softmax) / channel (epilogue)
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+
+  for (int t = 0; t < 5; ++t) {
+    // ---------------------------------------------------------------- build the key tile
+    if (t == 4) {
+      const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
+      for (int c = tid; c < 128 * 64; c += kAttnThreads) {
+        const uint32_t r = c >> 6, ch = c & 63;
+        const bool ok = static_cast<int32_t>(r) < wl;
+        cp_async16(smem_u32(Kt + tile_off(r, ch * 8)), ok ? static_cast<const void*>(wg + r * CSA2_D + ch * 8)
+                                                           : static_cast<const void*>(a.window),
+                   ok ? 16u : 0u);
+      }
+    } else {
+      int cnt_valid = 0;
+      {
+        int64_t p;
+        int32_t e;
+        const bool v = tid < 128 && key_valid(a, qi, t, tid, nv, wl, &p, &e);
+        if (tid < 128) {
+          const int32_t raw = __ldg(a.topk_idx + qi * CSA2_TOPK + t * 128 + tid);
+          if (raw >= 0 && !v) report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
+        }
+        cnt_valid = __syncthreads_count(v);
+      }
+      if (cnt_valid == 0) continue;  // block-uniform: nothing selected in this tile
+      uint4 nib[8];
+      uint32_t scw[8];
+      bool val[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int task = tid + kAttnThreads * i;
+        const int slot = task >> 4, j = task & 15;
+        int64_t p = 0;
+        int32_t e = 0;
+        val[i] = key_valid(a, qi, t, slot, nv, wl, &p, &e);
+        if (val[i]) {
+          const uint8_t* rec = a.cache.kv + p * kKvPageBytes + static_cast<int64_t>(e % kPage) * kKvBytes;
+          nib[i] = __ldg(reinterpret_cast<const uint4*>(rec) + j);
+          scw[i] = __ldg(reinterpret_cast<const uint16_t*>(rec + 256) + j);
+        } else {
+          nib[i] = make_uint4(0, 0, 0, 0);
+          scw[i] = 0;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int task = tid + kAttnThreads * i;
+        const uint32_t slot = task >> 4, j = task & 15;
+        const __nv_bfloat162 s0 = e4m3_bf16x2(scw[i] & 0xFFu), s1 = e4m3_bf16x2(scw[i] >> 8);
+        const uint32_t wds[4] = {nib[i].x, nib[i].y, nib[i].z, nib[i].w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          uint32_t o[4];
+          dequant8_bf16(wds[m], m < 2 ? s0 : s1, o);
+          *reinterpret_cast<uint4*>(Kt + tile_off(slot, 32 * j + 8 * m)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---------------------------------------------------------------- S^T = K Q^T
+    if (tid == 0) {
+      const uint32_t kb = smem_u32(Kt), qb = smem_u32(Qs);
+#pragma unroll 4
+      for (uint32_t kk = 0; kk < 32; ++kk)
+        mma_bf16(tmem + kSCols, sdesc(kb + kk * 256u, 128, 8192), sdesc(qb + kk * 256u, 128, 8192), idesc_s, kk);
+      mma_commit(mma_bar);
+      if (!mbar_wait(mma_bar, phase, nullptr)) {
+        flags[0] = 1;
+        report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
+      }
+    }
+    phase ^= 1;
+    __syncthreads();
+    tc_fence_after();
+    if (flags[0]) break;
+
+    // ---------------------------------------------------------------- softmax
+    bool kv_ok;
+    {
+      int64_t p;
+      int32_t e;
+      kv_ok = key_valid(a, qi, t, static_cast<int>(key_row), nv, wl, &p, &e);
+    }
+    float x[32];
+    {
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_base + kSCols + static_cast<uint32_t>(hb), r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = kv_ok ? __uint_as_float(r[i]) * a.scale_log2 : -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float m = redux_max(x[i]);
+      if (lane == i) tmax[(warp & 3) * kHeads + hb + i] = m;
+    }
+    if (tid == 0) flags[1] = 0;
+    __syncthreads();
+    if (tid < kHeads) {
+      const float mt = fmaxf(fmaxf(tmax[tid], tmax[kHeads + tid]), fmaxf(tmax[2 * kHeads + tid], tmax[3 * kHeads + tid]));
+      const float old = ref[tid];
+      float nw = old;
+      if (mt > old + kRescaleThreshold || (old == -INFINITY && mt != -INFINITY)) nw = mt;
+      alpha[tid] = (old == -INFINITY) ? 0.0f : exp2f(old - nw);
+      ref[tid] = nw;
+      if (nw != old && old != -INFINITY) flags[1] = 1;
+    }
+    __syncthreads();
+    if (flags[1] && o_started) {
+      // rescale O^T columns (heads) and the running sums by alpha
+#pragma unroll
+      for (int i = 0; i < 32; ++i) lsum[i] *= alpha[hb + i];
+      for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
+        for (int h0 = 0; h0 < 64; h0 += 32) {
+          uint32_t r[32];
+          const uint32_t addr = tmem + lane_base + kOCols + static_cast<uint32_t>(c * 64 + h0);
+          tmem_ld32(addr, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha[h0 + i]);
+          tmem_st32(addr, r);
+        }
+      }
+      tmem_st_wait();
+    }
+    // P = exp2(x - ref) -> bf16, P^T tile (MN-major: 8 heads x 2 bytes per core row)
+    {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float r0 = ref[hb + i], r1 = ref[hb + i + 1];
+        const float p0 = (r0 == -INFINITY) ? 0.0f : exp2f(x[i] - r0);
+        const float p1 = (r1 == -INFINITY) ? 0.0f : exp2f(x[i + 1] - r1);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        lsum[i] += __low2float(pb);
+        lsum[i + 1] += __high2float(pb);
+        pk[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t off = (key_row >> 3) * 1024u + static_cast<uint32_t>((hb >> 3) + c) * 128u + (key_row & 7u) * 16u;
+        *reinterpret_cast<uint4*>(Ps + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---------------------------------------------------------------- O^T += V^T P^T
+    if (tid == 0) {
+      const uint32_t kb = smem_u32(Kt), pb = smem_u32(Ps);
+      for (uint32_t c = 0; c < 4; ++c) {
+#pragma unroll
+        for (uint32_t kk = 0; kk < 8; ++kk) {
+          mma_bf16(tmem + kOCols + c * 64u, sdesc(kb + c * 2048u + kk * 16384u, 8192, 128),
+                   sdesc(pb + kk * 2048u, 1024, 128), idesc_o, (o_started || kk > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(mma_bar);
+      if (!mbar_wait(mma_bar, phase, nullptr)) {
+        flags[0] = 1;
+        report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
+      }
+    }
+    phase ^= 1;
+    o_started = true;
+    __syncthreads();
+    tc_fence_after();
+    if (flags[0]) break;
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  if (!flags[0]) {
+    // row sums: reduce the 128 key slots of each head
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float v = lsum[i];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == i) lred[(warp & 3) * kHeads + hb + i] = v;
+    }
+    __syncthreads();
+    if (tid < kHeads) {
+      const float l = lred[tid] + lred[kHeads + tid] + lred[2 * kHeads + tid] + lred[3 * kHeads + tid];
+      alpha[tid] = l;  // reuse: final row sum
+      if (a.lse) a.lse[qi * kHeads + tid] = (l > 0.0f) ? (ref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
+    __nv_bfloat16* og = a.out + qi * kHeads * CSA2_D;
+    for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
+      const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
+      for (int h0 = 0; h0 < 64; h0 += 32) {
+        uint32_t r[32];
+        if (o_started) {
+          tmem_ld32(tmem + lane_base + kOCols + static_cast<uint32_t>(c * 64 + h0), r);
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float l = alpha[h0 + i];
+          const float o = (o_started && l > 0.0f) ? __uint_as_float(r[i]) / l : 0.0f;
+          og[static_cast<int64_t>(h0 + i) * CSA2_D + d] = __float2bfloat16_rn(o);
+        }
+      }
+    }
+  }
+  // drain outstanding MMAs, then free TMEM
+  if (tid == 0) {
+    mma_commit(drain);
+    mbar_wait(drain, 0, nullptr);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+size_t attn_smem_bytes() {
+  return 1024 + kKtBytes + kQsBytes + kPsBytes + (2 + 8) * kHeads * sizeof(float) + 64;
+}
+
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
+  if (a.n_q == 0) return cudaSuccess;
+  const size_t smem = attn_smem_bytes();
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  attn_kernel<<<static_cast<unsigned>(a.n_q), kAttnThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,99 @@
+// k_pack.cu -- FP4 packing of new cache entries and of the indexer query.
+//
+// "DeepSeek's Attention and KV Cache - From MLA to CSA2", "DeepSeek-V4.1 ... Four bits
+// for the main KV": E2M1 elements with one E4M3 scale per 16 channels, the scale
+// mapping the block maximum onto 6, no tensor-level scale; 288 B per 512-channel
+// entry.  "DeepSeek-V4.1-Flash and the 890-byte KV cache", section 3: the 128-channel
+// indexer key in the same format, 72 B.  "DeepSeek-V4: ... The indexer in four bits":
+// the indexer query-key product runs entirely in FP4, so the query is packed with the
+// same codec.
+//
+// One thread per 16-channel block: two 16-byte loads, one fp32 division for the
+// scale, 16 for the codes (hardware RN/satfinite conversions), an 8-byte nibble
+// store and a 1-byte scale store.
+#include "csa2_kernels.cuh"
+
+namespace csa2 {
+
+__device__ __forceinline__ void load16(const __nv_bfloat16* src, float (&x)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+  const uint4 a = __ldg(p), b = __ldg(p + 1);
+  const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(u[i] << 16);
+    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+// Items [0, n_new*40) pack cache entries (32 main-KV blocks + 8 indexer blocks per
+// entry); items [n_new*40, +n_groups*128*8) pack indexer-query rows (rows >= N of a
+// group only clear their scale bytes).
+__global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t n_pack = a.n_new * 40;
+  if (item < n_pack) {
+    const int64_t i = item / 40;
+    const int b = static_cast<int>(item % 40);
+    const int32_t r = a.new_req[i];
+    const int64_t s = a.new_pos[i];
+    if (r < 0 || s < 0 || s >= static_cast<int64_t>(a.cache.max_pages) * kPage) {
+      report(a.err, CSA2_ERR_DEVICE, kInfoPos);
+      return;
+    }
+    const int64_t p = page_id(a.cache, r, s);
+    if (p < 0 || p >= a.cache.n_pages) {
+      report(a.err, CSA2_ERR_DEVICE, kInfoPage);
+      return;
+    }
+    const uint32_t e = static_cast<uint32_t>(s % kPage);
+    float x[16];
+    uint32_t lo, hi;
+    if (b < 32) {
+      load16(a.latent + i * kD + 16 * b, x);
+      const uint32_t sc = quant_block16(x, lo, hi);
+      uint8_t* rec = a.cache.kv + p * kKvPageBytes + static_cast<int64_t>(e) * kKvBytes;
+      *reinterpret_cast<uint2*>(rec + 8 * b) = make_uint2(lo, hi);
+      rec[256 + b] = static_cast<uint8_t>(sc);
+    } else {
+      const int bb = b - 32;
+      load16(a.idx_key + i * kDI + 16 * bb, x);
+      const uint32_t sc = quant_block16(x, lo, hi);
+      uint8_t* pg = a.cache.idx + p * kIdxPageBytes;
+      *reinterpret_cast<uint2*>(pg + idx_nib_off(e, bb)) = make_uint2(lo, hi);
+      pg[idx_sf_off(kIdxNibBytes, e, bb)] = static_cast<uint8_t>(sc);
+    }
+    return;
+  }
+  const int64_t qi = item - n_pack;
+  if (qi >= a.n_groups * 128 * 8) return;
+  const int64_t g = qi / (128 * 8);
+  const uint32_t n = static_cast<uint32_t>((qi / 8) % 128);
+  const uint32_t bb = static_cast<uint32_t>(qi % 8);
+  uint8_t* gp = a.qpack + g * a.grp_bytes;
+  const uint32_t nib_bytes = static_cast<uint32_t>(a.N) * 64u;
+  if (n >= static_cast<uint32_t>(a.N)) {  // unused scale slots of a short group
+    gp[idx_sf_off(nib_bytes, n, bb)] = 0;
+    return;
+  }
+  const int64_t q = g * a.G + n / a.heads_I;
+  const int32_t j = static_cast<int32_t>(n % a.heads_I);
+  uint32_t lo = 0, hi = 0, sc = 0;
+  if (q < a.n_q) {
+    float x[16];
+    load16(a.q_idx + (q * a.heads_I + j) * kDI + 16 * bb, x);
+    sc = quant_block16(x, lo, hi);
+  }
+  *reinterpret_cast<uint2*>(gp + idx_nib_off(n, bb)) = make_uint2(lo, hi);
+  gp[idx_sf_off(nib_bytes, n, bb)] = static_cast<uint8_t>(sc);
+}
+
+cudaError_t launch_pack(const PackArgs& a, cudaStream_t stream) {
+  const int64_t items = a.n_new * 40 + a.n_groups * 128 * 8;
+  if (items == 0) return cudaSuccess;
+  const int64_t blocks = (items + 255) / 256;
+  pack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,318 @@
+// k_topk.cu -- top-k selection over index scores.
+//
+// "DeepSeek's Attention and KV Cache - From MLA to CSA2", "DeepSeek-V3.2": selection is
+// a top-k over the index scores; "DeepSeek-V4.1": k = 512.  "From MLA to DSA to
+// HCA/CSA", "CSA: two changes to HCA": fewer than k visible entries leave -1 sentinels.
+//
+// Scores become order-preserving 32-bit keys (+0 and -0 equal).  Three launches, no
+// inter-CTA waiting:
+//   hist    (chunks x rows CTAs): 2048-bin histogram of the key's top 11 bits, smem
+//           atomics, merged into a per-row global histogram;
+//   select  (chunks x rows CTAs): every CTA derives the threshold bin b* (the bin that
+//           holds the k-th largest key) from the row histogram, appends indices with a
+//           higher bin to the row's selection and (key, index) pairs of bin b* to the
+//           row's candidate list (warp-aggregated atomics);
+//   final   (one CTA per row): sorts the candidates by (key desc, index asc), takes
+//           the k - |selection| first, merges, sorts the k indices ascending, pads -1.
+//           A row whose threshold bin overflows the candidate buffer (massive ties) is
+//           resolved by exact radix refinement over the whole row instead.
+// The result is unique: the k largest keys, equal keys by lower index.
+#include "csa2_kernels.cuh"
+
+namespace csa2 {
+
+constexpr int kBins = 2048;
+constexpr int kChunk = 32768;
+constexpr int kCandCap = 4096;
+constexpr int kTopkThreads = 512;
+
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0u) u = 0u;  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ int64_t row_visible(const TopkArgs& a, int64_t q) {
+  int64_t nv = __ldg(a.n_visible + q);
+  if (nv < 0) nv = 0;
+  if (nv > a.t_max) nv = a.t_max;
+  return nv;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(const TopkArgs a) {
+  __shared__ uint32_t h[kBins];
+  const int64_t q = blockIdx.y;
+  const int64_t nv = row_visible(a, q);
+  if (nv <= a.k) return;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+  if (c0 >= nv) return;
+  const int64_t c1 = c0 + kChunk < nv ? c0 + kChunk : nv;
+  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
+  __syncthreads();
+  const float* row = a.scores + q * a.ld;
+  const int64_t v1 = c0 + ((c1 - c0) & ~int64_t(3));
+  for (int64_t i = c0 + 4 * threadIdx.x; i < v1; i += 4 * kTopkThreads) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(row + i));
+    atomicAdd(&h[order_key(v.x) >> 21], 1u);
+    atomicAdd(&h[order_key(v.y) >> 21], 1u);
+    atomicAdd(&h[order_key(v.z) >> 21], 1u);
+    atomicAdd(&h[order_key(v.w) >> 21], 1u);
+  }
+  for (int64_t i = v1 + threadIdx.x; i < c1; i += kTopkThreads) atomicAdd(&h[order_key(__ldg(row + i)) >> 21], 1u);
+  __syncthreads();
+  uint32_t* gh = a.hist + q * kBins;
+  for (int b = threadIdx.x; b < kBins; b += kTopkThreads)
+    if (h[b]) atomicAdd(gh + b, h[b]);
+}
+
+// The bin holding the k-th largest key and the number of keys in higher bins.
+// h: smem histogram; 512 threads.
+__device__ void threshold_bin(const uint32_t* h, uint32_t k, int* s_bin, uint32_t* s_above, uint32_t* s_warp) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t loc = h[4 * t] + h[4 * t + 1] + h[4 * t + 2] + h[4 * t + 3];
+  uint32_t x = loc;  // inclusive suffix within the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t v = __shfl_down_sync(0xffffffffu, x, off);
+    if (lane + off < 32) x += v;
+  }
+  if (lane == 0) s_warp[warp] = x;
+  __syncthreads();
+  uint32_t higher = 0;
+  for (int w = warp + 1; w < kTopkThreads / 32; ++w) higher += s_warp[w];
+  uint32_t running = x - loc + higher;  // keys in bins above 4t+3
+  for (int b = 4 * t + 3; b >= 4 * t; --b) {
+    if (running < k && running + h[b] >= k) {
+      *s_bin = b;
+      *s_above = running;
+    }
+    running += h[b];
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void append(uint32_t* counter, bool pred, uint32_t& slot) {
+  const uint32_t m = __ballot_sync(0xffffffffu, pred);
+  if (m == 0) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(m)));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  slot = base + __popc(m & ((1u << lane) - 1u));
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(const TopkArgs a) {
+  __shared__ uint32_t h[kBins];
+  __shared__ uint32_t s_warp[32];
+  __shared__ int s_bin;
+  __shared__ uint32_t s_above;
+  const int64_t q = blockIdx.y;
+  const int64_t nv = row_visible(a, q);
+  if (nv <= a.k) return;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+  if (c0 >= nv) return;
+  const int64_t c1 = c0 + kChunk < nv ? c0 + kChunk : nv;
+  const uint32_t* gh = a.hist + q * kBins;
+  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = gh[b];
+  __syncthreads();
+  threshold_bin(h, static_cast<uint32_t>(a.k), &s_bin, &s_above, s_warp);
+  const uint32_t bstar = static_cast<uint32_t>(s_bin);
+  const float* row = a.scores + q * a.ld;
+  int32_t* sel = a.sel + q * a.k;
+  uint2* cand = a.cand + q * kCandCap;
+  // every lane of a warp runs the same number of iterations (ballots below)
+  for (int64_t base = c0; base < c1; base += kTopkThreads) {
+    const int64_t i = base + threadIdx.x;
+    uint32_t key = 0, bin = 0;
+    const bool in = i < c1;
+    if (in) {
+      key = order_key(__ldg(row + i));
+      bin = key >> 21;
+    }
+    uint32_t slot;
+    const bool hi = in && bin > bstar;
+    append(&a.cnt[2 * q], hi, slot);
+    if (hi && slot < static_cast<uint32_t>(a.k)) sel[slot] = static_cast<int32_t>(i);
+    const bool eq = in && bin == bstar;
+    append(&a.cnt[2 * q + 1], eq, slot);
+    if (eq && slot < kCandCap) cand[slot] = make_uint2(key, static_cast<uint32_t>(i));
+  }
+}
+
+// Bitonic sort, ascending, of n (power of two) elements in shared memory.
+template <typename T>
+__device__ void bitonic_sort(T* v, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = ((lo & size) == 0);
+        const T x = v[lo], y = v[hi];
+        if ((x > y) == up) {
+          v[lo] = y;
+          v[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Exact selection over a whole row by radix refinement (rows whose threshold bin
+// holds more than kCandCap keys).  Appends the chosen indices (beyond those already in
+// `picked[0..n_picked)`, which hold every index of a bin above b*) to `picked`.
+__device__ void refine_row(const TopkArgs& a, int64_t q, int64_t nv, uint32_t bstar, uint32_t need, uint32_t* h,
+                           uint32_t* s_warp, int32_t* picked, uint32_t* n_picked) {
+  __shared__ int s_bin;
+  __shared__ uint32_t s_above;
+  __shared__ uint32_t s_cnt;
+  const float* row = a.scores + q * a.ld;
+  uint32_t prefix = bstar, prefix_bits = 11;
+  // levels: bits [10, 21) then [0, 10) of the key below the 11-bit prefix
+  const int shifts[2] = {10, 0};
+  const int widths[2] = {11, 10};
+  for (int lv = 0; lv < 2; ++lv) {
+    const int sh = shifts[lv], wd = widths[lv];
+    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < nv; i += kTopkThreads) {
+      const uint32_t key = order_key(__ldg(row + i));
+      if ((key >> (32 - prefix_bits)) == prefix) atomicAdd(&h[(key >> sh) & ((1u << wd) - 1u)], 1u);
+    }
+    __syncthreads();
+    threshold_bin(h, need, &s_bin, &s_above, s_warp);
+    need -= s_above;
+    prefix = (prefix << wd) | static_cast<uint32_t>(s_bin);
+    prefix_bits += wd;
+  }
+  const uint32_t vstar = prefix;  // exact key of the k-th largest
+  // keys above vstar that are inside bin b* (higher bins are already picked)
+  for (int64_t base = 0; base < nv; base += kTopkThreads) {
+    const int64_t i = base + threadIdx.x;
+    const uint32_t key = i < nv ? order_key(__ldg(row + i)) : 0u;
+    const bool take = i < nv && (key >> 21) == bstar && key > vstar;
+    uint32_t slot;
+    append(n_picked, take, slot);
+    if (take && slot < static_cast<uint32_t>(a.k)) picked[slot] = static_cast<int32_t>(i);
+  }
+  // the `need` lowest indices whose key equals vstar, in index order
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  for (int64_t base = 0; base < nv; base += kTopkThreads) {
+    const int64_t i = base + threadIdx.x;
+    const bool eq = i < nv && order_key(__ldg(row + i)) == vstar;
+    const uint32_t m = __ballot_sync(0xffffffffu, eq);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) s_warp[warp] = __popc(m);
+    __syncthreads();
+    uint32_t before = s_cnt;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    const uint32_t rank = before + __popc(m & ((1u << lane) - 1u));
+    if (eq && rank < need) {
+      const uint32_t slot = atomicAdd(n_picked, 1u);
+      if (slot < static_cast<uint32_t>(a.k)) picked[slot] = static_cast<int32_t>(i);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int w = 0; w < kTopkThreads / 32; ++w) s_cnt += s_warp[w];
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(const TopkArgs a) {
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  uint64_t* cs = reinterpret_cast<uint64_t*>(tk_smem);                 // kCandCap composites
+  uint32_t* h = reinterpret_cast<uint32_t*>(cs + kCandCap);            // kBins
+  int32_t* picked = reinterpret_cast<int32_t*>(h + kBins);             // k (<= 512)
+  __shared__ uint32_t s_warp[32];
+  __shared__ int s_bin;
+  __shared__ uint32_t s_above;
+  __shared__ uint32_t n_picked;
+  const int64_t q = blockIdx.x;
+  const int64_t nv = row_visible(a, q);
+  int32_t* out = a.out + q * a.k;
+  if (nv <= a.k) {
+    for (int i = threadIdx.x; i < a.k; i += kTopkThreads) out[i] = i < nv ? i : -1;
+    return;
+  }
+  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = a.hist[q * kBins + b];
+  __syncthreads();
+  threshold_bin(h, static_cast<uint32_t>(a.k), &s_bin, &s_above, s_warp);
+  const uint32_t bstar = static_cast<uint32_t>(s_bin), above = s_above;
+  const uint32_t nc = h[bstar];
+  const uint32_t need = static_cast<uint32_t>(a.k) - above;
+  if (threadIdx.x == 0) {
+    if (a.cnt[2 * q] != above || a.cnt[2 * q + 1] != nc) report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
+    n_picked = above;
+  }
+  for (uint32_t i = threadIdx.x; i < above; i += kTopkThreads) picked[i] = a.sel[q * a.k + i];
+  __syncthreads();
+  if (nc <= kCandCap) {
+    int p2 = 1;
+    while (p2 < static_cast<int>(nc)) p2 <<= 1;
+    const uint2* cand = a.cand + q * kCandCap;
+    for (int i = threadIdx.x; i < p2; i += kTopkThreads) {
+      if (i < static_cast<int>(nc)) {
+        const uint2 c = cand[i];
+        cs[i] = (static_cast<uint64_t>(0xFFFFFFFFu - c.x) << 32) | c.y;
+      } else {
+        cs[i] = ~0ull;
+      }
+    }
+    __syncthreads();
+    bitonic_sort(cs, p2);
+    for (uint32_t i = threadIdx.x; i < need; i += kTopkThreads) picked[above + i] = static_cast<int32_t>(cs[i] & 0xFFFFFFFFu);
+    __syncthreads();
+  } else {
+    refine_row(a, q, nv, bstar, need, h, s_warp, picked, &n_picked);
+    __syncthreads();
+  }
+  // ascending order of the k chosen indices
+  bitonic_sort(picked, a.k);
+  for (int i = threadIdx.x; i < a.k; i += kTopkThreads) out[i] = picked[i];
+}
+
+size_t topk_final_smem() { return kCandCap * sizeof(uint64_t) + kBins * sizeof(uint32_t) + 512 * sizeof(int32_t); }
+
+size_t topk_ws_bytes(int64_t n_q) {
+  return static_cast<size_t>(n_q) * (kBins * 4 + 8 + 512 * 4 + kCandCap * 8);
+}
+
+void topk_carve(uint8_t* base, int64_t n_q, TopkArgs& a) {
+  a.hist = reinterpret_cast<uint32_t*>(base);
+  a.cnt = a.hist + n_q * kBins;
+  a.sel = reinterpret_cast<int32_t*>(a.cnt + 2 * n_q);
+  a.cand = reinterpret_cast<uint2*>(a.sel + 512 * n_q);
+}
+
+size_t topk_zero_bytes(int64_t n_q) { return static_cast<size_t>(n_q) * (kBins * 4 + 8); }
+
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream, int kind_hist, int kind_sel, int kind_final,
+                        TraceFn trace_begin, TraceFn trace_end) {
+  if (a.n_q == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(a.hist, 0, topk_zero_bytes(a.n_q), stream);
+  if (e != cudaSuccess) return e;
+  const int chunks = static_cast<int>((a.t_max + kChunk - 1) / kChunk);
+  if (chunks > 0) {
+    const dim3 grid(chunks, static_cast<unsigned>(a.n_q));
+    trace_begin(kind_hist, stream);
+    topk_hist_kernel<<<grid, kTopkThreads, 0, stream>>>(a);
+    trace_end(kind_hist, stream);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    trace_begin(kind_sel, stream);
+    topk_select_kernel<<<grid, kTopkThreads, 0, stream>>>(a);
+    trace_end(kind_sel, stream);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const size_t smem = topk_final_smem();
+  e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  trace_begin(kind_final, stream);
+  topk_final_kernel<<<static_cast<unsigned>(a.n_q), kTopkThreads, smem, stream>>>(a);
+  trace_end(kind_final, stream);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,219 @@
+/*
+ * csa2.h -- C ABI of libcsa2: one CSA2 attention layer (DeepSeek-V4.1-Flash) over an
+ * FP4 KV cache, at decode and chunked prefill, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page title, section):
+ *   [P1] "DeepSeek's Attention and KV Cache - From MLA to CSA2, From First Principles":
+ *        "A Precision Primer", "DeepSeek-V3.2: Sparse Attention With a Learned Indexer",
+ *        "DeepSeek-V4: Compress the Sequence, Then Sparsify",
+ *        "DeepSeek-V4.1: Reuse Across Layers, Project Across Halves, Store in Four Bits".
+ *   [P2] "From MLA to DSA to HCA/CSA: DeepSeek V3.2 and V4 Attention":
+ *        "The indexer", "What replaced MLA", "The sliding window", "CSA: two changes to HCA".
+ *   [P3] "DeepSeek-V4.1-Flash and the 890-byte KV cache", sections 2 and 3.
+ *   [P4] "From First Principles: DeepSeek-V4.1-Flash Inference":
+ *        "Two branches", "What's in a cell", "CSA2: four layers keep their own copy".
+ *
+ * Conventions for every entry point:
+ *   - Pointers named here are DEVICE pointers owned by the caller, unless stated.
+ *     The library allocates nothing; scratch memory is the caller's workspace `ws`
+ *     of `ws_bytes` bytes (see csa2_workspace_bytes), 256-byte aligned.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Argument validation is synchronous: a bad argument returns
+ *     CSA2_ERR_INVALID_ARG / CSA2_ERR_UNSUPPORTED / CSA2_ERR_WORKSPACE before anything
+ *     is launched, and csa2_last_error() gives a message.  A failed launch returns
+ *     CSA2_ERR_CUDA.  Limit breaches found on the device (a page id outside the cache,
+ *     a position beyond a request's pages, an index beyond the visible prefix, a
+ *     pipeline wait that ran out) skip the offending access and set an error word in
+ *     the workspace that csa2_check() reports (CSA2_ERR_DEVICE / CSA2_ERR_TIMEOUT).
+ *   - bf16 tensors are passed as `const void*` holding IEEE bfloat16 bit patterns.
+ *   - All device pointers must be 16-byte aligned; cache page arrays and the
+ *     workspace 256-byte aligned.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* csa2_stream_t; /* = cudaStream_t */
+
+typedef enum csa2_status {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1, /* a pointer, size or stride is invalid             */
+  CSA2_ERR_UNSUPPORTED = 2, /* a valid but unimplemented shape (e.g. k != 512) */
+  CSA2_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed            */
+  CSA2_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out              */
+  CSA2_ERR_WORKSPACE = 5,   /* ws is NULL, misaligned or smaller than needed   */
+  CSA2_ERR_DEVICE = 6       /* a device-side limit check failed (see csa2_check) */
+} csa2_status;
+
+/* Sizes fixed by the pages.
+ *   CSA2_D      main-KV latent width, 512 [P1 "DeepSeek-V4.1"; P2 "What replaced MLA"]
+ *   CSA2_DI     indexer key/query width, 128 [P1 "DeepSeek-V3.2"; P2 "The indexer"]
+ *   CSA2_BLOCK  channels per E4M3 scale, 16 [P1 "DeepSeek-V4.1": E2M1 with one E4M3
+ *               scale per 16 channels, NVFP4 without its global scale]
+ *   CSA2_KV_BYTES  256 B of nibbles + 32 scale bytes = 288 [P1 "DeepSeek-V4.1"]
+ *   CSA2_IDX_BYTES 64 B of nibbles + 8 scale bytes = 72 [P3 section 3]
+ *   CSA2_TOPK   selected entries per query, 512 [P1 "DeepSeek-V4.1"; P3 section 2]
+ *   CSA2_WIN    sliding-window entries, 128 [P1 "DeepSeek-V4"; P4 "Two branches"]
+ *   CSA2_HEADS  attention query heads sharing one KV entry, 64 [P2 "Part 2"; P4]
+ * Layout choice of this library (the pages give entry sizes only):
+ *   CSA2_PAGE   entries per cache page, 128. */
+enum {
+  CSA2_D = 512,
+  CSA2_DI = 128,
+  CSA2_BLOCK = 16,
+  CSA2_KV_BYTES = 288,
+  CSA2_IDX_BYTES = 72,
+  CSA2_TOPK = 512,
+  CSA2_WIN = 128,
+  CSA2_HEADS = 64,
+  CSA2_PAGE = 128,
+  CSA2_KV_PAGE_BYTES = 36864,  /* 128 x 288 */
+  CSA2_IDX_PAGE_BYTES = 9216   /* 128 x 72  */
+};
+
+/* The global cache of one CSA2 Full layer: a paged main-KV cache and a paged
+ * indexer-K cache sharing one block table [P1 "DeepSeek-V4": compressed entries are a
+ * classical paged cache; P4 "What's in a cell": main KV + indexer K per entry].
+ *
+ * Entry s of request r lives in page p = block_table[r*max_pages + s/128] (or
+ * p = r*max_pages + s/128 when block_table is NULL), slot e = s % 128.
+ *
+ * Main-KV page (36864 B): entry e occupies bytes [288e, 288e+288): byte i < 256 holds
+ *   channel 2i in its low nibble and channel 2i+1 in its high nibble (E2M1 codes:
+ *   bit 3 sign, bits 0-2 magnitude index of 0,.5,1,1.5,2,3,4,6); bytes 256..287 hold
+ *   the E4M3 scale of channels [16b, 16b+16) at byte 256+b.
+ * Indexer-K page (9216 B = 128 x 72): the nibble of entry e, channel c sits at byte
+ *   (e/8)*512 + (c/32)*128 + (e%8)*16 + (c%32)/2 (low nibble = even c): eight entries
+ *   form a 512-byte group of four 128-byte core blocks, the operand layout of the
+ *   block-scaled tensor-core MMA, so a page feeds the MMA without reshuffling.  The
+ *   E4M3 scale of entry e, block b sits at byte 8192 + (b/4)*512 + (e%32)*16 +
+ *   (e/32)*4 + b%4, the scale-factor layout the MMA reads.
+ * Each entry still costs exactly 288 + 72 bytes. */
+typedef struct csa2_cache {
+  uint8_t* kv;                /* main-KV pages [n_pages][36864]                     */
+  uint8_t* idx;               /* indexer-K pages [n_pages][9216]                    */
+  const int32_t* block_table; /* [n_req][max_pages] page ids, or NULL (contiguous)  */
+  int32_t max_pages;          /* pages per request (row length of block_table)      */
+  int32_t n_pages;            /* pages allocated in kv and idx (bounds check)       */
+} csa2_cache;
+
+/* One CSA2 layer step for n_q queries [P1 "DeepSeek-V4.1" three modes; P3 section 2;
+ * P4 "CSA2"].  Query q belongs to request req[q], sees entries [0, n_visible[q]) of
+ * that request's cache, and attends to the topk selected entries plus its window
+ * rows window[(win_start[q] + i) * 512 ...] for i < win_len[q] (<= 128). */
+typedef struct csa2_step {
+  int64_t n_q;               /* number of queries (decode: one per request)            */
+  int32_t heads;             /* attention heads, must be 64                            */
+  int32_t heads_I;           /* indexer heads: 64 or 32                                */
+  int32_t topk;              /* must be 512                                            */
+  int32_t group;             /* indexer query group: 1, or 2 when consecutive queries
+                                share one request (chunked prefill)                    */
+  int64_t t_max;             /* host-known upper bound of n_visible[] (grid sizing)    */
+  const void* q;             /* bf16 [n_q][heads][512], post-RoPE attention queries    */
+  const void* q_idx;         /* bf16 [n_q][heads_I][128] indexer queries (Full/Reindex)*/
+  const float* w;            /* fp32 [n_q][heads_I] indexer head weights               */
+  const int32_t* req;        /* [n_q] request of each query                            */
+  const int32_t* n_visible;  /* [n_q] visible cache entries of each query              */
+  const void* window;        /* bf16 window rows [*][512]                              */
+  const int64_t* win_start;  /* [n_q] first window row of each query                   */
+  const int32_t* win_len;    /* [n_q] window rows of each query, 0..128                */
+  int64_t n_new;             /* Full mode: entries to pack before scoring (may be 0)   */
+  const void* new_latent;    /* bf16 [n_new][512] main-KV latents (post-RoPE)          */
+  const void* new_idx_key;   /* bf16 [n_new][128] indexer keys                         */
+  const int32_t* new_req;    /* [n_new] request of each new entry                      */
+  const int64_t* new_pos;    /* [n_new] position of each new entry in its request      */
+  csa2_cache cache;          /* the (possibly shared) global cache                     */
+  int32_t* topk_idx;         /* [n_q][topk]: output (Full, Reindex) or input (Reuse);
+                                ascending entry indices, -1 padded                     */
+  float* scores;             /* optional fp32 [n_q][ld] index scores out; NULL = keep
+                                them in the workspace                                  */
+  int64_t ld;                /* row stride of scores (elements, multiple of 4) or 0    */
+  float softmax_scale;       /* <= 0 selects 512^-0.5                                  */
+  void* out;                 /* bf16 [n_q][heads][512] attention output                */
+  float* lse;                /* optional fp32 [n_q][heads] natural-log sum-exp         */
+} csa2_step;
+
+/* Message describing the last failed call on this host thread ("" if none). */
+const char* csa2_last_error(void);
+
+/* Workspace bytes needed by every call below for n_q queries of up to t_max visible
+ * entries with heads_I indexer heads; scores_in_ws != 0 when the caller does not
+ * provide a score array (the scores then live in the workspace).  Host-only. */
+size_t csa2_workspace_bytes(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws);
+
+/* Pack n new entries into the cache [P1 "DeepSeek-V4.1", Four bits for the main KV;
+ * P3 section 3].  For each 16-channel block: amax = max|x|, scale =
+ * E4M3_rn_satfinite(amax / 6) (fp32 division), code_i = E2M1_rn_satfinite(x_i / scale)
+ * (fp32 division; a zero scale gives +0 codes).  latent: bf16 [n][512]; idx_key: bf16
+ * [n][128]; req/pos: [n].  Entries at the same (req, pos) must not repeat in one call. */
+csa2_status csa2_pack_kv(const void* latent, const void* idx_key, const int32_t* req,
+                         const int64_t* pos, int64_t n, const csa2_cache* cache, void* ws,
+                         size_t ws_bytes, csa2_stream_t stream);
+
+/* Lightning-indexer scores [P1 "DeepSeek-V3.2" index score, "DeepSeek-V4" the indexer
+ * in four bits; P2 "The indexer", "CSA" scorer]:
+ *   scores[q*ld + s] = sum_j w[q][j] * ReLU( qhat[q][j] . khat[s] * 128^-0.5 )
+ * for s < n_visible[q], where qhat is q_idx quantised in-call with the same E2M1/E4M3
+ * block codec and khat the cached indexer key (the product runs on the block-scaled
+ * FP4 tensor cores, fp32 accumulation).  Entries s >= n_visible[q] are not written.
+ * group = 1 or 2 consecutive queries of one request per MMA tile. */
+csa2_status csa2_index_score(const void* q_idx, const float* w, int32_t heads_I,
+                             const int32_t* req, const int32_t* n_visible, int64_t n_q,
+                             int32_t group, int64_t t_max, const csa2_cache* cache,
+                             float* scores, int64_t ld, void* ws, size_t ws_bytes,
+                             csa2_stream_t stream);
+
+/* Top-k selection [P1 "DeepSeek-V3.2" top-k, "DeepSeek-V4.1" top-512; P2 "CSA" -1
+ * sentinel]: for each row q the k largest of scores[q*ld + s], s < n_visible[q];
+ * equal scores prefer the lower index, -0 equals +0; out_idx[q][0..k) lists the chosen
+ * indices in ascending order, padded with -1 when n_visible[q] < k.  k must be 512. */
+csa2_status csa2_topk(const float* scores, int64_t ld, const int32_t* n_visible, int64_t n_q,
+                      int64_t t_max, int32_t k, int32_t* out_idx, void* ws, size_t ws_bytes,
+                      csa2_stream_t stream);
+
+/* Full mode [P3 section 2 "Full Mode"; P4 "CSA2"]: pack the step's new entries, score
+ * the cache with the step's own indexer query, select its own top-512, then run the
+ * shared-KV MQA over the 512 selected (dequantised) entries plus the window rows:
+ *   for each head h: S = scale * Q_h . K^T over keys K = [selected ; window] (K == V),
+ *   O_h = softmax(S) K, lse_h = log sum exp S   [P1 "DeepSeek-V4"; P2 "What replaced MLA"].
+ * Window and selection may overlap; nothing is de-duplicated. */
+csa2_status csa2_sparse_attn_full(const csa2_step* step, void* ws, size_t ws_bytes,
+                                  csa2_stream_t stream);
+
+/* Reindex mode [P3 section 2 "Reindex Mode"]: as Full mode on a cache written by
+ * another layer (no packing): its own indexer query, its own top-512, then attention. */
+csa2_status csa2_sparse_attn_reindex(const csa2_step* step, void* ws, size_t ws_bytes,
+                                     csa2_stream_t stream);
+
+/* Reuse mode [P3 section 2 "Reuse Mode"]: attention only, over step->topk_idx given by a
+ * preceding Full or Reindex layer plus the window rows; no indexer work. */
+csa2_status csa2_sparse_attn_reuse(const csa2_step* step, void* ws, size_t ws_bytes,
+                                   csa2_stream_t stream);
+
+/* Synchronise `stream`, read and clear the workspace error word.  Returns CSA2_OK,
+ * CSA2_ERR_DEVICE or CSA2_ERR_TIMEOUT; *info (may be NULL) receives a code naming the
+ * check that failed (1 page id, 2 position, 3 top-k index, 4 group request, 5 wait). */
+csa2_status csa2_check(void* ws, csa2_stream_t stream, int32_t* info);
+
+/* Number of kernels this library has launched in this process. */
+int64_t csa2_launch_count(void);
+
+/* Per-kernel device timing with CUDA events recorded on the launching stream.
+ * csa2_trace_enable(1) starts recording (at most 4096 launches are kept);
+ * csa2_trace_read(kind, &ms, &n) synchronises and returns the summed duration and count
+ * of kernel `kind` (0 pack/quantise, 1 index score, 2 top-k histogram, 3 top-k select,
+ * 4 top-k final, 5 attention); csa2_trace_enable(0) stops and clears. */
+csa2_status csa2_trace_enable(int32_t on);
+csa2_status csa2_trace_read(int32_t kind, double* total_ms, int64_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H_ */

@@ -17,3 +17,13 @@ def orc():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def csa2():
+    from fp4_compressed_sparse_csa2_gb300 import build
+    build.build()
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from fp4_compressed_sparse_csa2_gb300 import csa2 as lib
+    return lib

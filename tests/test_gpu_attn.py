@@ -1,0 +1,83 @@
+"""Sparse + window MQA parity (Reuse mode, given indices): bf16 output within 2e-2
+max-abs of the fp64 oracle ("DeepSeek's Attention and KV Cache", "DeepSeek-V4": 512
+selected entries concatenated with the 128 window entries, one shared vector as key and
+value; "From MLA to DSA to HCA/CSA", "What replaced MLA": K and V are the same tensor)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from helpers import Cache, dev, dev_bf16, fill_cache
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+def _reuse(orc, csa2, n_entries, idx, req_q, win_len, seed, qscale=1.0, win_rows=None):
+    n_req = len(n_entries)
+    max_pages = (max(n_entries) + 127) // 128
+    cache = Cache(n_req, max_pages)
+    lat, key, req_e, pos_e = fill_cache(cache, n_entries, seed)
+    kv_h, ix_h = orc.alloc_pages(cache.n_pages)
+    orc.pack_kv(lat, key, req_e, pos_e, kv_h, ix_h, None, max_pages)
+    n_q = len(req_q)
+    q = synth.normal_bf16(seed + 3, (n_q, 64, 512), scale=qscale)
+    nwin = win_rows or 128 * n_q
+    window = synth.normal_bf16(seed + 4, (nwin, 512))
+    win_start = np.array([128 * i if win_rows is None else i for i in range(n_q)], np.int64)
+    win_len = np.array(win_len, np.int32)
+    nvis = np.array([n_entries[r] for r in req_q], np.int32)
+    out = torch.zeros((n_q, 64, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((n_q, 64), dtype=torch.float32, device="cuda")
+    topk_idx = dev(np.ascontiguousarray(idx, np.int32))
+    step = csa2.make_step(n_q=n_q, t_max=int(max(n_entries)), q=dev_bf16(q), req=dev(np.array(req_q, np.int32)),
+                          n_visible=dev(nvis), window=dev_bf16(window), win_start=dev(win_start),
+                          win_len=dev(win_len), cache=cache.c, topk_idx=topk_idx, out=out, lse=lse)
+    ws = csa2.alloc_workspace(n_q, 64, int(max(n_entries)), False)
+    csa2.sparse_attn_reuse(step, ws)
+    assert csa2.check(ws) == (csa2.OK, 0)
+    O = out.float().cpu().numpy()
+    L = lse.cpu().numpy()
+    for i in range(n_q):
+        ws_ = int(win_start[i])
+        Oref, lref = orc.attention(q[i], idx[i], kv_h, int(req_q[i]), window[ws_:ws_ + max(1, win_len[i])],
+                                   int(win_len[i]), None, None, max_pages)
+        err = np.abs(O[i] - Oref).max()
+        assert err <= TOL, (i, err)
+        fin = np.isfinite(lref)
+        assert np.array_equal(fin, np.isfinite(L[i]))
+        assert np.abs(L[i][fin] - lref[fin]).max() <= 1e-2
+    return O
+
+
+def test_attn_reuse_random_indices(orc, csa2):
+    n = [2000, 900]
+    idx = np.stack([synth.distinct_indices(1, 2000, 512), synth.distinct_indices(2, 900, 512)])
+    _reuse(orc, csa2, n, idx, [0, 1], [128, 128], seed=50)
+
+
+def test_attn_padding_window_lengths_and_duplicates(orc, csa2):
+    n = [700, 300]
+    a = synth.distinct_indices(3, 300, 512)          # 300 valid + 212 x -1
+    b = np.full(512, -1, np.int32)                   # window only
+    c = synth.distinct_indices(4, 700, 512)
+    c[:64] = c[64:128]                               # duplicates are attended twice
+    d = np.full(512, -1, np.int32)
+    d[:3] = [5, 6, 699]
+    idx = np.stack([a, b, c, d])
+    _reuse(orc, csa2, n, idx, [1, 0, 0, 0], [128, 57, 1, 0], seed=51)
+
+
+def test_attn_peaky_queries(orc, csa2):
+    """Q x 8 makes the softmax peaky, so the 2e-2 bound is a real constraint."""
+    n = [1500]
+    idx = np.stack([synth.distinct_indices(5, 1500, 512), synth.distinct_indices(6, 1500, 512)])
+    _reuse(orc, csa2, n, idx, [0, 0], [128, 100], seed=52, qscale=8.0)
+
+
+def test_attn_shared_window_rows_prefill_style(orc, csa2):
+    """Consecutive queries share a window buffer with shifted starts (chunked prefill)."""
+    n = [1200]
+    n_q = 3
+    idx = np.stack([synth.distinct_indices(10 + i, 1200, 512) for i in range(n_q)])
+    _reuse(orc, csa2, n, idx, [0] * n_q, [128, 128, 128], seed=53, win_rows=130)
