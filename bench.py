@@ -1,0 +1,425 @@
+"""Benchmark of one CSA2 attention layer (DeepSeek-V4.1-Flash) at decode on GB300.
+
+Metric: CSA2 decode layer-steps/s at 128K context (Full mode: pack the new entry of every
+request, score all 131,072 cached entries per request with the FP4 lightning indexer,
+select the top-512, attend over them plus a 128-row bf16 window with 64 heads), and the
+achieved HBM GB/s of the dominant kernel against the measured copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line is printed by rank 0.  Under torchrun each rank runs its own batch of
+requests (weak scaling; decode requests are independent, so there is no collective on
+the data path); the timed region is bracketed by a barrier and a device synchronise and
+the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "CSA2 decode layer-steps/s at 128K ctx; achieved HBM GB/s vs 8 TB/s"
+UNIT = "layer-steps/s"
+HEADS, HEADS_I, D, DI, TOPK, WIN = 64, 64, 512, 128, 512, 128
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--batch", type=int, default=64, help="requests per GPU (the workload uses 64)")
+    p.add_argument("--ctx", type=int, default=131072, help="cached entries per request (the workload uses 131072)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def workload_name(B, T):
+    return f"Full-mode decode, batch {B} requests x 1 query, T={T} cached entries (ratio-1 decoder cache), " \
+           f"top-512, window 128, 64 attention heads, 64 indexer heads"
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        self.gpu = ids[gpu_index] if gpu_index < len(ids) else str(gpu_index)
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+class Workload:
+    """Seeded synthetic Full-mode decode step resident on the device."""
+
+    def __init__(self, B: int, T: int, rank: int, device):
+        import synth
+        from fp4_compressed_sparse_csa2_gb300 import csa2
+        self.csa2 = csa2
+        self.B, self.T, self.dev = B, T, device
+        self.max_pages = (T + 127) // 128
+        n_pages = B * self.max_pages
+        self.kv = torch.empty(n_pages * csa2.KV_PAGE_BYTES, dtype=torch.uint8, device=device)
+        self.idx = torch.empty(n_pages * csa2.IDX_PAGE_BYTES, dtype=torch.uint8, device=device)
+        self.cache = csa2.make_cache(self.kv, self.idx, self.max_pages)
+        ws0 = csa2.alloc_workspace(1, 64, 0, False, device)
+        base = 1000 * 1 + 100000 * rank          # per-request seed = 1000*config + request (+ rank offset)
+        pos = torch.arange(T - 1, dtype=torch.int64, device=device)
+        for r in range(B):
+            lat = synth.torch_normal_bf16(base + r, (T - 1, D), device)
+            key = synth.torch_normal_bf16(base + r + 50000, (T - 1, DI), device)
+            req = torch.full((T - 1,), r, dtype=torch.int32, device=device)
+            csa2.pack_kv(lat, key, req, pos, self.cache, ws0)
+            del lat, key
+        sb = base + 7_000_000
+        self.q = synth.torch_normal_bf16(sb + 1, (B, HEADS, D), device)
+        self.q_idx = synth.torch_normal_bf16(sb + 2, (B, HEADS_I, DI), device)
+        self.w = synth.torch_normal_f32(sb + 3, (B, HEADS_I), device)
+        self.new_lat = synth.torch_normal_bf16(sb + 4, (B, D), device)
+        self.new_key = synth.torch_normal_bf16(sb + 5, (B, DI), device)
+        self.window = synth.torch_normal_bf16(sb + 6, (B * WIN, D), device)
+        self.req = torch.arange(B, dtype=torch.int32, device=device)
+        self.nvis = torch.full((B,), T, dtype=torch.int32, device=device)
+        self.win_start = torch.arange(B, dtype=torch.int64, device=device) * WIN
+        self.win_len = torch.full((B,), WIN, dtype=torch.int32, device=device)
+        self.new_req = torch.arange(B, dtype=torch.int32, device=device)
+        self.new_pos = torch.full((B,), T - 1, dtype=torch.int64, device=device)
+        self.topk_idx = torch.empty((B, TOPK), dtype=torch.int32, device=device)
+        self.out = torch.empty((B, HEADS, D), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((B, HEADS), dtype=torch.float32, device=device)
+        self.ws = csa2.alloc_workspace(B, HEADS_I, T, True, device)
+        self.step = self.make_step(self.q, self.q_idx, self.w, self.new_lat, self.new_key, self.out)
+        torch.cuda.synchronize()
+
+    def make_step(self, q, q_idx, w, new_lat, new_key, out):
+        return self.csa2.make_step(
+            n_q=self.B, t_max=self.T, q=q, req=self.req, n_visible=self.nvis, window=self.window,
+            win_start=self.win_start, win_len=self.win_len, cache=self.cache, topk_idx=self.topk_idx, out=out,
+            lse=self.lse, q_idx=q_idx, w=w, heads_I=HEADS_I, group=1, n_new=self.B, new_latent=new_lat,
+            new_idx_key=new_key, new_req=self.new_req, new_pos=self.new_pos)
+
+    def run(self, step=None):
+        self.csa2.sparse_attn_full(step or self.step, self.ws)
+
+    # bytes the step must read from HBM (indexer keys, selected entries, window rows)
+    def must_read_bytes(self):
+        return self.B * (self.T * 72 + TOPK * 288 + WIN * D * 2)
+
+
+# ----------------------------------------------------------------------------- oracle sample
+def oracle_sample(wl: "Workload", n_req: int, threads: int):
+    """Time the CPU oracle on the Full-mode step of n_req requests (pack of the new entry,
+    index scores over all T entries, top-512, attention); returns (seconds, requests)."""
+    import oracle as orc
+    import synth
+    B, T = wl.B, wl.T
+    base = 1000 * 1
+    reqs = list(range(min(n_req, B)))
+    host = {}
+    for r in reqs:   # the same seeded inputs, regenerated on the device and copied to the host
+        lat = synth.torch_normal_bf16(base + r, (T - 1, D), wl.dev)
+        key = synth.torch_normal_bf16(base + r + 50000, (T - 1, DI), wl.dev)
+        host[r] = (lat.view(torch.int16).cpu().numpy().view(np.uint16), key.view(torch.int16).cpu().numpy().view(np.uint16))
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    q, q_idx, w = bits(wl.q), bits(wl.q_idx), wl.w.cpu().numpy()
+    new_lat, new_key, window = bits(wl.new_lat), bits(wl.new_key), bits(wl.window)
+    caches = {}
+
+    def build(r):    # the resident cache, built outside the timed region
+        kv, ix = orc.alloc_pages(wl.max_pages)
+        lat, key = host[r]
+        orc.pack_kv(lat, key, np.zeros(T - 1, np.int32), np.arange(T - 1, dtype=np.int64), kv, ix, None,
+                    wl.max_pages)
+        caches[r] = (kv, ix)
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(build, reqs))
+
+    def one(r):
+        kv, ix = caches[r]
+        orc.pack_kv(new_lat[r:r + 1], new_key[r:r + 1], np.zeros(1, np.int32), np.array([T - 1], np.int64), kv, ix,
+                    None, wl.max_pages)
+        I, _ = orc.index_score(q_idx[r], w[r], ix, 0, 0, T, None, wl.max_pages)
+        sel = orc.topk(I.astype(np.float32), TOPK)
+        orc.attention(q[r], sel, kv, 0, window[WIN * r:WIN * (r + 1)], WIN, None, None, wl.max_pages)
+        return sel
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, reqs))
+    return time.perf_counter() - t0, len(reqs)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- arms
+def run_ours(args, ws, rank, local):
+    dev = torch.device("cuda", local)
+    from fp4_compressed_sparse_csa2_gb300 import csa2
+    wl = Workload(args.batch, args.ctx, rank, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        wl.run()
+    st, info = csa2.check(wl.ws)
+    assert st == csa2.OK, f"device error word {st} info {info}"
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        # untimed soak so that the sampler (200 ms period) sees the GPU under this load
+        t_end = time.time() + 1.5
+        while time.time() < t_end:
+            for _ in range(20):
+                wl.run()
+            torch.cuda.synchronize()
+        barrier(ws)
+        torch.cuda.synchronize()
+        csa2.trace_enable(True)
+        l0 = csa2.launch_count()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            wl.run()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        launches = csa2.launch_count() - l0
+    barrier(ws)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    kernels = {}
+    for k in csa2.TRACE_KINDS:
+        tot, n = csa2.trace_read(k)
+        if n:
+            kernels[k] = {"us_per_launch": 1000 * tot / n, "launches": n}
+    csa2.trace_enable(False)
+    st, info = csa2.check(wl.ws)
+    assert st == csa2.OK, f"device error word {st} info {info}"
+    ms = max_over_ranks(ms, ws)
+    value = ws / (ms / 1000.0)
+
+    # roofline of the dominant kernel (the indexer): algorithmic bytes = 72 B per scored entry
+    idx_us = kernels["index"]["us_per_launch"]
+    idx_bytes = wl.B * wl.T * 72
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = idx_bytes / (idx_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": "index_kernel", "achieved": round(achieved, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks else "fallback 6.8 TB/s",
+                "traffic": None, "algorithmic_bytes": idx_bytes}
+    step_gbs = wl.must_read_bytes() / (ms * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()
+        hq, hqi, hw, hl, hk = pin(wl.q), pin(wl.q_idx), pin(wl.w), pin(wl.new_lat), pin(wl.new_key)
+        hout = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+        dq, dqi, dw, dl, dk = (torch.empty_like(x) for x in (wl.q, wl.q_idx, wl.w, wl.new_lat, wl.new_key))
+        dout = torch.empty_like(wl.out)
+        step = wl.make_step(dq, dqi, dw, dl, dk, dout)
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hqi, hw, hl, hk))
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            for d_, h_ in ((dq, hq), (dqi, hqi), (dw, hw), (dl, hl), (dk, hk)):
+                d_.copy_(h_, non_blocking=True)
+            wl.run(step)
+            hout.copy_(dout, non_blocking=True)
+
+        for _ in range(max(args.warmup, 3)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws)
+        e2e = {"value": round(ws / (ems / 1000.0), 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ems, 4)}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cores = host_cores()
+        n_req = min(wl.B, max(4, cores))
+        secs, nr = oracle_sample(wl, n_req, cores)
+        cpu = {"value": round((nr / wl.B) / secs, 6), "unit": UNIT, "cores": min(cores, nr), "kind": "oracle",
+               "sample": f"{nr} of {wl.B} requests of the same Full-mode step (pack + fp64 index scores over "
+                         f"{wl.T} entries + top-512 + fp64 attention), {secs:.2f} s wall on {min(cores, nr)} "
+                         f"threads, scaled to one {wl.B}-request layer-step"}
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp4e2m1 x fp4e2m1 (indexer), bf16 (attention), fp32 acc",
+            "data": "synthetic (seeded N(0,1) latents, keys, queries; fp32 N(0,1) head weights)",
+            "config": {"workload": workload_name(wl.B, wl.T), "global_batch": wl.B * ws, "seq_len": wl.T,
+                       "parallelism": f"replicas x{ws} (requests sharded, no collective)",
+                       "l2": "inputs larger than L2: 604 MB of indexer keys per step stream from HBM"},
+            "hbm": {"must_read_bytes_per_step": wl.must_read_bytes(), "step_gbs": round(step_gbs, 1),
+                    "frac_of_8tbs": round(step_gbs / NOMINAL_HBM_GBS, 4),
+                    "frac_of_measured": round(step_gbs / hbm_peak, 4)},
+            "roofline": roofline,
+            "kernels": {k: {"us_per_launch": round(v["us_per_launch"], 2), "launches": v["launches"]}
+                        for k, v in kernels.items()},
+            "gpu_launches": int(launches),
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, ws, rank, local):
+    """The oracle as it stands, on the host cores, timed per step on a bounded sample."""
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else None
+    if dev is None:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm builds its inputs on the GPU"}))
+        return
+    wl = Workload(args.batch, args.ctx, 0, dev)
+    cores = host_cores()
+    n_req = min(wl.B, max(2, cores // 2))
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_sample(wl, 1, 1)
+    times = []
+    for _ in range(max(1, min(args.steps, 3))):
+        secs, nr = oracle_sample(wl, n_req, cores)
+        times.append(secs * wl.B / nr)      # seconds per full 64-request layer-step
+    sec = statistics.median(times)
+    value = 1.0 / sec
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": ws, "steps": len(times),
+        "warmup": max(0, min(args.warmup, 1)), "ms_per_step": round(sec * 1000, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+        "data": "synthetic (seeded N(0,1)), same inputs as the GPU arm",
+        "config": {"workload": workload_name(wl.B, wl.T), "global_batch": wl.B, "seq_len": wl.T},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": min(cores, n_req), "kind": "oracle",
+                         "sample": f"{n_req} of {wl.B} requests per step, scaled to one {wl.B}-request layer-step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, ws, rank, local)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -165,11 +165,10 @@ csa2_status run_index(const csa2_cache& cache, const uint8_t* qpack, const float
   a.n_groups = (n_q + G - 1) / G;
   a.tpg = static_cast<int32_t>((t_max + kPage - 1) / kPage);
   a.err = err;
-  const bool small = a.N <= 64;
-  a.stages = small ? 6 : 12;
-  a.tmem_cols = small ? 256u : 512u;
+  a.stages = 16;
+  a.tmem_cols = 512u;
   const int64_t total = a.n_groups * a.tpg;
-  const int64_t slots = static_cast<int64_t>(sm_count()) * (small ? 2 : 1);
+  const int64_t slots = static_cast<int64_t>(sm_count());  // one persistent CTA per SM
   const int grid = static_cast<int>(total < slots ? total : slots);
   trace_begin(kIndex, stream);
   const cudaError_t e = launch_index(a, grid, stream);

@@ -72,15 +72,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase.  Returns false (and never blocks longer than
-// kWaitLimitNs) when the phase did not complete or *abort became non-zero.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  A waiting thread is parked by the hardware
+// (suspend-time hint) instead of spinning, so waiting warps leave the issue slots to
+// the warps that work; the wall-clock bound is checked every 16 polls.  Returns false
+// (after at most about kWaitLimitNs) when the phase did not complete or *abort became
+// non-zero.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (abort != nullptr && *abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 

@@ -121,22 +121,40 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(const TopkArg
   const float* row = a.scores + q * a.ld;
   int32_t* sel = a.sel + q * a.k;
   uint2* cand = a.cand + q * kCandCap;
-  // every lane of a warp runs the same number of iterations (ballots below)
-  for (int64_t base = c0; base < c1; base += kTopkThreads) {
-    const int64_t i = base + threadIdx.x;
-    uint32_t key = 0, bin = 0;
-    const bool in = i < c1;
-    if (in) {
-      key = order_key(__ldg(row + i));
-      bin = key >> 21;
+  // uniform trip count so that the warp votes below see every lane; 4 keys per thread
+  const int64_t n_iter = (c1 - c0 + 4 * kTopkThreads - 1) / (4 * kTopkThreads);
+  for (int64_t it = 0; it < n_iter; ++it) {
+    const int64_t i0 = c0 + it * 4 * kTopkThreads + 4 * threadIdx.x;
+    uint32_t key[4], bin[4];
+    bool in[4];
+    if (i0 + 3 < c1) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(row + i0));
+      key[0] = order_key(v.x); key[1] = order_key(v.y); key[2] = order_key(v.z); key[3] = order_key(v.w);
+      in[0] = in[1] = in[2] = in[3] = true;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        in[j] = i0 + j < c1;
+        key[j] = in[j] ? order_key(__ldg(row + i0 + j)) : 0u;
+      }
     }
-    uint32_t slot;
-    const bool hi = in && bin > bstar;
-    append(&a.cnt[2 * q], hi, slot);
-    if (hi && slot < static_cast<uint32_t>(a.k)) sel[slot] = static_cast<int32_t>(i);
-    const bool eq = in && bin == bstar;
-    append(&a.cnt[2 * q + 1], eq, slot);
-    if (eq && slot < kCandCap) cand[slot] = make_uint2(key, static_cast<uint32_t>(i));
+    bool any = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      bin[j] = key[j] >> 21;
+      any |= in[j] && bin[j] >= bstar;
+    }
+    if (!__any_sync(0xffffffffu, any)) continue;  // the common case: nothing to keep here
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t slot;
+      const bool hi = in[j] && bin[j] > bstar;
+      append(&a.cnt[2 * q], hi, slot);
+      if (hi && slot < static_cast<uint32_t>(a.k)) sel[slot] = static_cast<int32_t>(i0 + j);
+      const bool eq = in[j] && bin[j] == bstar;
+      append(&a.cnt[2 * q + 1], eq, slot);
+      if (eq && slot < kCandCap) cand[slot] = make_uint2(key[j], static_cast<uint32_t>(i0 + j));
+    }
   }
 }
 
