@@ -62,6 +62,8 @@ def _load():
     L.csa2_topk.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp, sz, vp]
     for f in ("csa2_sparse_attn_full", "csa2_sparse_attn_reindex", "csa2_sparse_attn_reuse"):
         getattr(L, f).argtypes = [ctypes.POINTER(csa2_step), vp, sz, vp]
+    L.csa2_topk_noalloc.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp]
+    L.csa2_topk_noalloc.restype = ctypes.c_int
     L.csa2_check.argtypes = [vp, vp, ctypes.POINTER(i32)]
     L.csa2_launch_count.restype = i64
     L.csa2_trace_enable.argtypes = [i32]
@@ -123,6 +125,12 @@ def index_score(q_idx, w, heads_I, req, n_visible, n_q, group, t_max, cache, sco
 def topk(scores, ld, n_visible, n_q, t_max, k, out_idx, ws, stream=None):
     _check(lib.csa2_topk(_ptr(scores), int(ld), _ptr(n_visible), int(n_q), int(t_max), int(k), _ptr(out_idx),
                          _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def topk_noalloc(scores, ld, n_visible, n_q, t_max, k, out_idx, stream=None):
+    """csa2_topk without a workspace: scratch is a fixed array inside the library (n_q <= 128)."""
+    _check(lib.csa2_topk_noalloc(_ptr(scores), int(ld), _ptr(n_visible), int(n_q), int(t_max), int(k),
+                                 _ptr(out_idx), _stream(stream)))
 
 
 def make_step(*, n_q, t_max, q, req, n_visible, window, win_start, win_len, cache, topk_idx, out, q_idx=None,

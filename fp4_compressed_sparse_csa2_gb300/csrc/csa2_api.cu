@@ -402,3 +402,28 @@ csa2_status csa2_trace_read(int32_t kind, double* total_ms, int64_t* count) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// csa2_topk_noalloc: the top-k of csa2_topk with its scratch in a fixed device array
+// inside the library instead of a caller workspace, for callers that cannot allocate
+// device memory.  It allocates nothing.
+extern "C" csa2_status csa2_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_visible, int64_t n_q,
+                                         int64_t t_max, int32_t k, int32_t* out_idx, csa2_stream_t stream) {
+  if (n_q < 0 || t_max < 0) return fail(CSA2_ERR_INVALID_ARG, "n_q and t_max must be >= 0");
+  if (n_q > kStaticTopkRows)
+    return fail(CSA2_ERR_WORKSPACE, "csa2_topk_noalloc handles at most %lld rows per call (got %lld)",
+                static_cast<long long>(kStaticTopkRows), static_cast<long long>(n_q));
+  if (k != CSA2_TOPK) return fail(CSA2_ERR_UNSUPPORTED, "k must be 512 (got %d)", k);
+  if (n_q > 0 && (!scores || !n_visible || !out_idx || ld < t_max || ld % 4 != 0 || !aligned(scores, 16)))
+    return fail(CSA2_ERR_INVALID_ARG, "scores (16-byte aligned, ld >= t_max, ld %% 4 == 0), n_visible and out_idx are required");
+  uint8_t* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  cudaError_t e = topk_static_scratch(&scratch, &scratch_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_topk_noalloc scratch lookup");
+  if (scratch_bytes < kHeader + topk_ws_bytes(n_q)) return fail(CSA2_ERR_WORKSPACE, "static top-k scratch too small");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the error word starts clear on every call; the histograms are cleared by the launch
+  e = cudaMemsetAsync(scratch, 0, kHeader, s);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_topk_noalloc");
+  return run_topk(scores, ld, n_visible, n_q, t_max, k, out_idx, scratch + kHeader, err_word(scratch), s);
+}

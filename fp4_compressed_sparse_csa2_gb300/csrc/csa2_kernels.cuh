@@ -86,6 +86,11 @@ size_t topk_ws_bytes(int64_t n_q);
 void topk_carve(uint8_t* base, int64_t n_q, TopkArgs& a);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream, int kind_hist, int kind_sel, int kind_final,
                         TraceFn trace_begin, TraceFn trace_end);
+// No-allocation top-k: rows held by the fixed scratch, and its device address on the
+// current device (looked up on first use per device).
+constexpr int64_t kStaticTopkRows = 128;
+constexpr int kMaxDevices = 64;
+cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes);
 size_t attn_smem_bytes();
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
 

@@ -17,6 +17,8 @@
 //           A row whose threshold bin overflows the candidate buffer (massive ties) is
 //           resolved by exact radix refinement over the whole row instead.
 // The result is unique: the k largest keys, equal keys by lower index.
+#include <mutex>
+
 #include "csa2_kernels.cuh"
 
 namespace csa2 {
@@ -331,6 +333,38 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream, int kind_hist, i
   topk_final_kernel<<<static_cast<unsigned>(a.n_q), kTopkThreads, smem, stream>>>(a);
   trace_end(kind_final, stream);
   return cudaGetLastError();
+}
+
+}  // namespace csa2
+
+// ----------------------------------------------------------------------------
+// Fixed scratch for the no-allocation top-k entry point (csa2_topk_noalloc).
+// A file-scope device array: every GPU that loads the library holds it until the
+// process exits.  Host code cannot pass the array's name to a kernel (on the host it
+// is only a stand-in symbol), so the device address is looked up once per device with
+// cudaGetSymbolAddress and cached.
+namespace csa2 {
+
+constexpr size_t kStaticScratchBytes = 256 + static_cast<size_t>(kStaticTopkRows) * (kBins * 4 + 8 + 512 * 4 + kCandCap * 8);
+static __device__ __align__(256) uint8_t g_topk_scratch[kStaticScratchBytes];
+
+cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes) {
+  static std::mutex mu;
+  static uint8_t* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_topk_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<uint8_t*>(p);
+  }
+  *ptr = addr[dev];
+  *bytes = kStaticScratchBytes;
+  return cudaSuccess;
 }
 
 }  // namespace csa2

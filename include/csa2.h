@@ -177,6 +177,25 @@ csa2_status csa2_topk(const float* scores, int64_t ld, const int32_t* n_visible,
                       int64_t t_max, int32_t k, int32_t* out_idx, void* ws, size_t ws_bytes,
                       csa2_stream_t stream);
 
+/* No-allocation variant of csa2_topk (the pages have no counterpart to this entry point).
+ * Some callers cannot call cudaMalloc: a serving engine that hands all device memory to
+ * its KV-cache pool at start-up, or a host thread that must not stall, since
+ * cudaMalloc and cudaFree can synchronise the device.  This call takes no workspace:
+ * its scratch is a fixed device array inside the library, sized for at most 128 rows
+ * (n_q <= 128, about 5.5 MB, held on every GPU that loads the library until the
+ * process exits).  It allocates nothing and calls no allocating routine.
+ *   - Same arguments and result as csa2_topk; n_q > 128 returns CSA2_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents behind (the
+ *     parts that must start at zero are cleared by each call): calls whose work
+ *     overlaps on the GPU (different streams, or different host threads) race and
+ *     must be serialised by the caller.
+ *   - Device-side checks write the array's own error word, not a caller workspace, so
+ *     csa2_check does not report them. */
+csa2_status csa2_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_visible, int64_t n_q,
+                              int64_t t_max, int32_t k, int32_t* out_idx, csa2_stream_t stream);
+
 /* Full mode [P3 section 2 "Full Mode"; P4 "CSA2"]: pack the step's new entries, score
  * the cache with the step's own indexer query, select its own top-512, then run the
  * shared-KV MQA over the 512 selected (dequantised) entries plus the window rows:
