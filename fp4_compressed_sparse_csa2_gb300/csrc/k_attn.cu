@@ -29,7 +29,7 @@ constexpr int kHeads = 64;
 constexpr uint32_t kKtBytes = 128 * 512 * 2;   // bf16 key tile
 constexpr uint32_t kQsBytes = 64 * 512 * 2;    // bf16 queries
 constexpr uint32_t kPsBytes = 128 * 64 * 2;    // bf16 P^T
-constexpr uint32_t kOCols = 0, kSCols = 256;   // TMEM columns
+constexpr uint32_t kOCols = 0, kSCols = 256;   // TMEM columns: O^T 4 x 64, S^T 4 partial sums x 64
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 
 // Offset of element (row, col) in a [rows][512] bf16 operand tile stored as 8x8 core
@@ -54,21 +54,6 @@ __device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
   return __nv_bfloat162(b, b);
 }
 
-// Key validity of entry `slot` of tile `t` (t < 4: selected, t == 4: window).
-__device__ __forceinline__ bool key_valid(const AttnArgs& a, int64_t qi, int t, int slot, int32_t nv, int32_t wl,
-                                          int64_t* page_out, int32_t* e_out) {
-  if (t == 4) return slot < wl;
-  const int32_t e = __ldg(a.topk_idx + qi * CSA2_TOPK + t * 128 + slot);
-  if (e < 0) return false;
-  if (e >= nv) return false;
-  const int32_t r = __ldg(a.req + qi);
-  const int64_t p = page_id(a.cache, r, e);
-  if (p < 0 || p >= a.cache.n_pages) return false;
-  *page_out = p;
-  *e_out = e;
-  return true;
-}
-
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -79,10 +64,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   float* alpha = ref + kHeads;                            // [64]
   float* tmax = alpha + kHeads;                           // [4][64]
   float* lred = tmax + 4 * kHeads;                        // [4][64]
-  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(lred + 4 * kHeads);
+  int64_t* recoff = reinterpret_cast<int64_t*>(lred + 4 * kHeads);     // [512] record byte offsets, -1 = none
+  int32_t* tile_cnt = reinterpret_cast<int32_t*>(recoff + CSA2_TOPK);  // [4] valid entries per selected tile
+  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(tile_cnt + 4);
   uint64_t* drain = mma_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  int32_t* flags = reinterpret_cast<int32_t*>(tmem_slot + 1);  // [0] abort, [1] rescale, [2] count
+  int32_t* flags = reinterpret_cast<int32_t*>(tmem_slot + 1);  // [0] abort, [1] rescale
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t qi = blockIdx.x;
@@ -107,6 +94,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     for (int c = tid; c < kHeads * 64; c += kAttnThreads) {
       const uint32_t h = c >> 6, ch = c & 63;
       cp_async16(smem_u32(Qs + tile_off(h, ch * 8)), qg + h * CSA2_D + ch * 8, 16);
+    }
+  }
+  // offsets of the 512 selected records (one round trip for all indices)
+  if (tid < 4) tile_cnt[tid] = 0;
+  __syncthreads();
+  {
+    const int32_t r = __ldg(a.req + qi);
+    for (int i = tid; i < CSA2_TOPK; i += kAttnThreads) {
+      const int32_t e = __ldg(a.topk_idx + qi * CSA2_TOPK + i);
+      int64_t off = -1;
+      if (e >= 0) {
+        const int64_t pg = e < nv ? page_id(a.cache, r, e) : -1;
+        if (pg >= 0 && pg < a.cache.n_pages)
+          off = pg * kKvPageBytes + static_cast<int64_t>(e % kPage) * kKvBytes;
+        else
+          report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
+      }
+      recoff[i] = off;
+      if (off >= 0) atomicAdd(&tile_cnt[i >> 7], 1);
     }
   }
   tc_fence_before();
@@ -137,36 +143,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
                    ok ? 16u : 0u);
       }
     } else {
-      int cnt_valid = 0;
-      {
-        int64_t p;
-        int32_t e;
-        const bool v = tid < 128 && key_valid(a, qi, t, tid, nv, wl, &p, &e);
-        if (tid < 128) {
-          const int32_t raw = __ldg(a.topk_idx + qi * CSA2_TOPK + t * 128 + tid);
-          if (raw >= 0 && !v) report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
-        }
-        cnt_valid = __syncthreads_count(v);
-      }
-      if (cnt_valid == 0) continue;  // block-uniform: nothing selected in this tile
+      if (tile_cnt[t] == 0) continue;  // block-uniform: nothing selected in this tile
       uint4 nib[8];
       uint32_t scw[8];
-      bool val[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int task = tid + kAttnThreads * i;
         const int slot = task >> 4, j = task & 15;
-        int64_t p = 0;
-        int32_t e = 0;
-        val[i] = key_valid(a, qi, t, slot, nv, wl, &p, &e);
-        if (val[i]) {
-          const uint8_t* rec = a.cache.kv + p * kKvPageBytes + static_cast<int64_t>(e % kPage) * kKvBytes;
-          nib[i] = __ldg(reinterpret_cast<const uint4*>(rec) + j);
-          scw[i] = __ldg(reinterpret_cast<const uint16_t*>(rec + 256) + j);
-        } else {
-          nib[i] = make_uint4(0, 0, 0, 0);
-          scw[i] = 0;
-        }
+        const int64_t off = recoff[t * 128 + slot];
+        const uint8_t* rec = a.cache.kv + (off >= 0 ? off : 0);
+        nib[i] = off >= 0 ? __ldg(reinterpret_cast<const uint4*>(rec) + j) : make_uint4(0, 0, 0, 0);
+        scw[i] = off >= 0 ? __ldg(reinterpret_cast<const uint16_t*>(rec + 256) + j) : 0u;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -192,8 +179,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     if (tid == 0) {
       const uint32_t kb = smem_u32(Kt), qb = smem_u32(Qs);
 #pragma unroll 4
-      for (uint32_t kk = 0; kk < 32; ++kk)
-        mma_bf16(tmem + kSCols, sdesc(kb + kk * 256u, 128, 8192), sdesc(qb + kk * 256u, 128, 8192), idesc_s, kk);
+      for (uint32_t kk = 0; kk < 32; ++kk)  // kk % 4 picks one of four independent partial sums
+        mma_bf16(tmem + kSCols + (kk & 3u) * 64u, sdesc(kb + kk * 256u, 128, 8192), sdesc(qb + kk * 256u, 128, 8192),
+                 idesc_s, kk >= 4 ? 1u : 0u);
       mma_commit(mma_bar);
       if (!mbar_wait(mma_bar, phase, nullptr)) {
         flags[0] = 1;
@@ -206,19 +194,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     if (flags[0]) break;
 
     // ---------------------------------------------------------------- softmax
-    bool kv_ok;
-    {
-      int64_t p;
-      int32_t e;
-      kv_ok = key_valid(a, qi, t, static_cast<int>(key_row), nv, wl, &p, &e);
-    }
+    const bool kv_ok = t == 4 ? static_cast<int32_t>(key_row) < wl : recoff[t * 128 + key_row] >= 0;
     float x[32];
     {
       uint32_t r[32];
       tmem_ld32(tmem + lane_base + kSCols + static_cast<uint32_t>(hb), r);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = kv_ok ? __uint_as_float(r[i]) * a.scale_log2 : -INFINITY;
+      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+#pragma unroll
+      for (uint32_t pp = 1; pp < 4; ++pp) {
+        tmem_ld32(tmem + lane_base + kSCols + pp * 64u + static_cast<uint32_t>(hb), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] += __uint_as_float(r[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = kv_ok ? x[i] * a.scale_log2 : -INFINITY;
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -281,9 +273,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     // ---------------------------------------------------------------- O^T += V^T P^T
     if (tid == 0) {
       const uint32_t kb = smem_u32(Kt), pb = smem_u32(Ps);
-      for (uint32_t c = 0; c < 4; ++c) {
+      for (uint32_t kk = 0; kk < 8; ++kk) {
 #pragma unroll
-        for (uint32_t kk = 0; kk < 8; ++kk) {
+        for (uint32_t c = 0; c < 4; ++c) {  // four independent accumulators interleaved
           mma_bf16(tmem + kOCols + c * 64u, sdesc(kb + c * 2048u + kk * 16384u, 8192, 128),
                    sdesc(pb + kk * 2048u, 1024, 128), idesc_o, (o_started || kk > 0) ? 1u : 0u);
         }
@@ -348,7 +340,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
 }
 
 size_t attn_smem_bytes() {
-  return 1024 + kKtBytes + kQsBytes + kPsBytes + (2 + 8) * kHeads * sizeof(float) + 64;
+  return 1024 + kKtBytes + kQsBytes + kPsBytes + (2 + 8) * kHeads * sizeof(float) + 64 + CSA2_TOPK * 8 + 16;
 }
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {

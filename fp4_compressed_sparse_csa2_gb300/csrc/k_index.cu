@@ -6,15 +6,15 @@
 // multiplies entirely in FP4.  "From MLA to DSA to HCA/CSA", "CSA: two changes to
 // HCA": the scorer takes ReLU(q . k) * 128^-0.5, weights it per head and sums heads.
 //
-// Design: one persistent CTA per SM (10 warps) over a contiguous range of 128-key
+// Design: one persistent CTA per SM (21 warps) over a contiguous range of 128-key
 // tiles (one indexer page each):
 //   warp 0      producer: one 9216-byte bulk copy per page (the page is stored in the
 //               MMA's operand layout) and one per packed query group, into a
 //               16-deep mbarrier ring (147 KB in flight per SM);
-//   warp 1      TMEM allocator and MMA issuer: tcgen05.cp of the E4M3 scale atoms,
+//   warps 1-4   TMEM allocator (warp 1) and four MMA issuers: tcgen05.cp of the E4M3 scale atoms,
 //               then two tcgen05.mma kind::mxf4nvf4 (K = 64 each) per tile into one of
 //               4 (N <= 64) or 2 (N = 128) fp32 TMEM accumulators D[128 keys][N];
-//   warps 2..9  two epilogue warpgroups taking alternate tiles: tcgen05.ld of one TMEM
+//   warps 5..20 four epilogue warpgroups taking every fourth tile: tcgen05.ld of one TMEM
 //               row per thread (thread = key), ReLU, head weights, head sum with four
 //               independent accumulators, x 128^-0.5, coalesced fp32 stores.
 // Every wait is bounded; a timeout sets the workspace error word, and the CTA drains
@@ -23,8 +23,10 @@
 
 namespace csa2 {
 
-constexpr int kIdxThreads = 352;  // producer, MMA issuer 0, 8 epilogue warps, MMA issuer 1
-constexpr int kIdxStages = 16;
+constexpr uint32_t kIssuers = 4;    // MMA-issuing warps
+constexpr uint32_t kEpiGroups = 4;  // epilogue warpgroups
+constexpr int kIdxThreads = 32 * (1 + kIssuers + 4 * kEpiGroups);  // producer, issuers, epilogue
+constexpr int kIdxStages = 16;  // ring capacity in pages (147 KB); a stage holds n_iss pages
 constexpr float kInvSqrtDI = 0.08838834764831845f;  // 128^-0.5
 
 // The CTA's range [begin, end) of the flat (group, tile) space, walked as group
@@ -68,25 +70,32 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
   constexpr int S = kIdxStages;
   uint8_t* ring = smem;                                                 // S x 9216
   uint8_t* qslot = ring + static_cast<size_t>(S) * kIdxPageBytes;       // 2 x 9216
-  float* sw_all = reinterpret_cast<float*>(qslot + 2 * kIdxPageBytes);  // 8 warps x 128 head weights
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sw_all + 8 * 128);
+  float* sw_all = reinterpret_cast<float*>(qslot + 2 * kIdxPageBytes);  // per epilogue warp: 128 head weights
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sw_all + 4 * kEpiGroups * 128);
   uint64_t* full = bars;               // [S]
   uint64_t* empty = full + S;          // [S]
   uint64_t* acc_full = empty + S;      // [4]
   uint64_t* acc_empty = acc_full + 4;  // [4]
   uint64_t* q_full = acc_empty + 4;    // [2]
   uint64_t* q_empty = q_full + 2;      // [2]
-  uint64_t* drain = q_empty + 2;       // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  uint64_t* drain = q_empty + 2;       // [kIssuers]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kIssuers);
   volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  volatile int32_t* go = abort + 1;  // [kEpiGroups][2] leader -> warpgroup hand-off
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t N = static_cast<uint32_t>(a.N);
   const int n_acc = N <= 64 ? 4 : 2;  // TMEM accumulators
+  // Accumulator b serves tiles n with n % n_acc == b.  Each accumulator must always be
+  // handled by the same issuer and the same epilogue warpgroup, so that no waiter can
+  // run two barrier phases ahead (parity waits would alias): the active issuer and
+  // warpgroup counts divide n_acc.
+  const uint32_t n_iss = kIssuers < static_cast<uint32_t>(n_acc) ? kIssuers : static_cast<uint32_t>(n_acc);
+  const uint32_t n_wg = kEpiGroups < static_cast<uint32_t>(n_acc) ? kEpiGroups : static_cast<uint32_t>(n_acc);
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&full[i], 1);       // the producer's one arrive per stage (plus the copies' bytes)
+      mbar_init(&empty[i], n_iss);  // one commit per issuer (one page each)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -94,10 +103,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 2);  // released by both MMA issuers
+      mbar_init(&q_empty[i], n_iss);  // released by every active MMA issuer
     }
-    mbar_init(&drain[0], 1);
-    mbar_init(&drain[1], 1);
+    for (uint32_t i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -121,9 +129,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      // Stage k holds the pages of tiles k*n_iss .. k*n_iss + n_iss - 1 (one per issuer);
+      // pages adjacent in memory go in one bulk copy.
       const uint64_t pol = policy_evict_first();
-      uint32_t s = 0, ph = 0, n_issued = 0, m = 0;
+      const uint32_t n_st = kIdxStages / n_iss;
+      uint32_t k = 0, ph = 0, in_st = 0, n_stages = 0, m = 0, run_len = 0;
+      int64_t run_page = 0;
+      uint8_t* run_dst = ring;
       bool ok = true;
+      auto flush = [&]() {
+        if (run_len) {
+          const uint32_t bytes = run_len * static_cast<uint32_t>(kIdxPageBytes);
+          mbar_expect_tx(&full[k], bytes);
+          bulk_g2s_hint(run_dst, a.idx_pages + run_page * kIdxPageBytes, bytes, &full[k], pol);
+          run_len = 0;
+        }
+      };
       Segment sg;
       for (int64_t g = g_first; ok && g <= g_last; ++g) {
         if (!segment(a, g, begin, end, sg)) continue;
@@ -137,39 +158,58 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
           ++m;
         }
         for (int32_t t = sg.t0; t < sg.t1; ++t) {
-          ok = mbar_wait(&empty[s], ph ^ 1u, abort);
-          if (!ok) break;
-          const int64_t page = seg_page(sg, t);
-          if (page >= 0 && page < a.cache.n_pages) {
-            mbar_arrive_expect_tx(&full[s], kIdxPageBytes);
-            bulk_g2s_hint(ring + s * kIdxPageBytes, a.idx_pages + page * kIdxPageBytes, kIdxPageBytes, &full[s],
-                          pol);
-          } else {
-            report(a.err, CSA2_ERR_DEVICE, kInfoPage);
-            mbar_arrive(&full[s]);
+          if (in_st == 0) {
+            ok = mbar_wait(&empty[k], ph ^ 1u, abort);
+            if (!ok) break;
           }
-          ++n_issued;
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
+          const int64_t page = seg_page(sg, t);
+          uint8_t* dst = ring + (k * n_iss + in_st) * kIdxPageBytes;
+          if (page >= 0 && page < a.cache.n_pages) {
+            if (run_len && page == run_page + run_len) {
+              ++run_len;
+            } else {
+              flush();
+              run_page = page;
+              run_len = 1;
+              run_dst = dst;
+            }
+          } else {
+            flush();
+            report(a.err, CSA2_ERR_DEVICE, kInfoPage);
+          }
+          if (++in_st == n_iss) {
+            flush();
+            mbar_arrive(&full[k]);
+            in_st = 0;
+            ++n_stages;
+            if (++k == n_st) {
+              k = 0;
+              ph ^= 1u;
+            }
           }
         }
+      }
+      if (ok && in_st) {  // partial last stage
+        flush();
+        mbar_arrive(&full[k]);
+        ++n_stages;
       }
       if (!ok) {
         *abort = 1;
         report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
       }
-      // the last copies issued into each slot land before the CTA exits
-      for (uint32_t k = (n_issued > S ? n_issued - S : 0); k < n_issued; ++k)
-        mbar_wait(&full[k % S], (k / S) & 1u, nullptr);
-      for (uint32_t k = (m > 2 ? m - 2 : 0); k < m; ++k) mbar_wait(&q_full[k & 1u], (k >> 1) & 1u, nullptr);
+      // the copies of the last stages land before the CTA exits
+      for (uint32_t j = (n_stages > n_st ? n_stages - n_st : 0); j < n_stages; ++j)
+        mbar_wait(&full[j % n_st], (j / n_st) & 1u, nullptr);
+      for (uint32_t j = (m > 2 ? m - 2 : 0); j < m; ++j) mbar_wait(&q_full[j & 1u], (j >> 1) & 1u, nullptr);
     }
-  } else if (warp == 1 || warp == 10) {
-    if (lane == 0) {
+  } else if (warp >= 1 && warp <= static_cast<int>(kIssuers)) {
+    if (lane == 0 && static_cast<uint32_t>(warp - 1) < n_iss) {
       // ------------------------------------------------------------ MMA issuers
-      // issuer i takes the tiles n with n % 2 == i (accumulators i and i + 2), so two
-      // threads on different sub-partitions hide each other's tcgen05 issue latency
-      const uint32_t me = warp == 1 ? 0u : 1u;
+      // issuer i takes the tiles n with n % n_iss == i: a single thread pays ~130 cycles per
+      // dependent tcgen05 op, so four issuers on different warps keep the tensor pipe and
+      // the copy ring moving
+      const uint32_t me = static_cast<uint32_t>(warp - 1);
       const uint32_t idesc = idesc_nvf4(128, a.N);
       uint32_t n = 0, m = 0, cur = 0;
       bool ok = true;
@@ -182,20 +222,21 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         if (!ok) break;
         tc_fence_after();
         const uint32_t qs = smem_u32(qslot + cur * kIdxPageBytes);
-        const uint32_t sfb = tmem + 288u + 16u * me + 8u * cur;
+        const uint32_t sfb = tmem + 288u + 16u * me + 8u * cur;  // 288..351
         tmem_cp_sf(sfb, sdesc(qs + nib_q, 128, 128));
         tmem_cp_sf(sfb + 4, sdesc(qs + nib_q + 512, 128, 128));
         ++m;
         for (int32_t t = sg.t0; t < sg.t1; ++t, ++n) {
-          if ((n & 1u) != me) continue;
-          const uint32_t s = n % S, ph = (n / S) & 1u;
+          if ((n & (n_iss - 1)) != me) continue;
+          const uint32_t kst = n / n_iss, n_st = kIdxStages / n_iss;
+          const uint32_t s = kst % n_st, ph = (kst / n_st) & 1u;
           const uint32_t b = n & static_cast<uint32_t>(n_acc - 1), bph = (n >> (n_acc == 4 ? 2 : 1)) & 1u;
           ok = mbar_wait(&full[s], ph, abort);
           if (!ok) break;
           ok = mbar_wait(&acc_empty[b], bph ^ 1u, abort);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t st = smem_u32(ring + s * kIdxPageBytes);
+          const uint32_t st = smem_u32(ring + (s * n_iss + me) * kIdxPageBytes);
           const uint32_t sfa = tmem + 256u + 8u * b;
           tmem_cp_sf(sfa, sdesc(st + kIdxNibBytes, 128, 128));
           tmem_cp_sf(sfa + 4, sdesc(st + kIdxNibBytes + 512, 128, 128));
@@ -216,16 +257,19 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // warpgroup wg takes every other tile; thread = TMEM lane = key of the tile
-    const uint32_t wg = static_cast<uint32_t>(warp - 2) >> 2;
+    // warpgroup wg takes the tiles with n % n_wg == wg; thread = TMEM lane = key
+    const uint32_t wg = static_cast<uint32_t>(warp - 1 - kIssuers) >> 2;
     const int quarter = warp & 3;
+    // one leader warp per warpgroup polls the accumulator barrier; the other three park
+    // on a named barrier and cost no issue slots while they wait
+    const bool leader = static_cast<uint32_t>(quarter) == ((wg + 1u) & 3u);
     const uint32_t row = static_cast<uint32_t>(quarter * 32 + lane);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float* sw = sw_all + (warp - 2) * 128;  // this warp's copy of the group's head weights
-    uint32_t n = 0, b = 0, bph = 0;
+    float* sw = sw_all + (warp - 1 - kIssuers) * 128;  // this warp's copy of the group's head weights
+    uint32_t n = 0, own = 0;
     bool ok = true;
     Segment sg;
-    for (int64_t g = g_first; ok && g <= g_last; ++g) {
+    for (int64_t g = g_first; ok && wg < n_wg && g <= g_last; ++g) {
       if (!segment(a, g, begin, end, sg)) continue;
       const int64_t q0 = g * a.G;
       __syncwarp();
@@ -236,19 +280,23 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
       }
       __syncwarp();
       const int nq = static_cast<int>(a.n_q - q0 < a.G ? a.n_q - q0 : a.G);
-      for (int32_t t = sg.t0; t < sg.t1; ++t) {
-        const bool mine = (n & 1u) == wg;
-        const uint32_t bb = b, bp = bph;
-        ++n;
-        if (++b == static_cast<uint32_t>(n_acc)) {
-          b = 0;
-          bph ^= 1u;
-        }
-        if (!mine) continue;
+      for (int32_t t = sg.t0; t < sg.t1; ++t, ++n) {
+        if ((n & (n_wg - 1)) != wg) continue;
+        const uint32_t bb = n & static_cast<uint32_t>(n_acc - 1);
+        const uint32_t bp = (n >> (n_acc == 4 ? 2 : 1)) & 1u;
         const int64_t page = seg_page(sg, t);
         const bool page_ok = page >= 0 && page < a.cache.n_pages;
-        ok = mbar_wait(&acc_full[bb], bp, abort);
-        if (!ok) break;
+        volatile int32_t* my_go = go + 2 * wg + (own & 1u);
+        ++own;
+        if (leader) {
+          const bool got = mbar_wait(&acc_full[bb], bp, abort);
+          if (lane == 0) *my_go = got ? 1 : 0;
+        }
+        named_bar_sync(1u + wg, 128u);
+        if (*my_go == 0) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const int32_t key = t * kPage + static_cast<int32_t>(row);
         for (int gq = 0; gq < nq; ++gq) {
@@ -287,8 +335,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
 
 size_t index_smem_bytes(int stages) {
   (void)stages;
-  return 1024 + static_cast<size_t>(kIdxStages + 2) * kIdxPageBytes + 8 * 128 * sizeof(float) +
-         (2 * kIdxStages + 14) * sizeof(uint64_t) + 16;
+  return 1024 + static_cast<size_t>(kIdxStages + 2) * kIdxPageBytes + 4 * kEpiGroups * 128 * sizeof(float) +
+         (2 * kIdxStages + 12 + kIssuers) * sizeof(uint64_t) + 16 + 4 * (2 + 2 * kEpiGroups);
 }
 
 cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream) {

@@ -24,7 +24,7 @@
 namespace csa2 {
 
 constexpr int kBins = 2048;
-constexpr int kChunk = 32768;
+constexpr int kChunk = 8192;  // score entries per CTA in the hist and select passes
 constexpr int kCandCap = 4096;
 constexpr int kTopkThreads = 512;
 
@@ -52,15 +52,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(const TopkArgs 
   for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
   __syncthreads();
   const float* row = a.scores + q * a.ld;
-  const int64_t v1 = c0 + ((c1 - c0) & ~int64_t(3));
-  for (int64_t i = c0 + 4 * threadIdx.x; i < v1; i += 4 * kTopkThreads) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(row + i));
-    atomicAdd(&h[order_key(v.x) >> 21], 1u);
-    atomicAdd(&h[order_key(v.y) >> 21], 1u);
-    atomicAdd(&h[order_key(v.z) >> 21], 1u);
-    atomicAdd(&h[order_key(v.w) >> 21], 1u);
+  if (c1 - c0 == kChunk) {  // full chunk: 4 float4 per thread, all loads in flight together
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const float4*>(row + c0) + threadIdx.x + u * kTopkThreads);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      atomicAdd(&h[order_key(v[u].x) >> 21], 1u);
+      atomicAdd(&h[order_key(v[u].y) >> 21], 1u);
+      atomicAdd(&h[order_key(v[u].z) >> 21], 1u);
+      atomicAdd(&h[order_key(v[u].w) >> 21], 1u);
+    }
+  } else {
+    for (int64_t i = c0 + threadIdx.x; i < c1; i += kTopkThreads) atomicAdd(&h[order_key(__ldg(row + i)) >> 21], 1u);
   }
-  for (int64_t i = v1 + threadIdx.x; i < c1; i += kTopkThreads) atomicAdd(&h[order_key(__ldg(row + i)) >> 21], 1u);
   __syncthreads();
   uint32_t* gh = a.hist + q * kBins;
   for (int b = threadIdx.x; b < kBins; b += kTopkThreads)
@@ -123,26 +128,31 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(const TopkArg
   const float* row = a.scores + q * a.ld;
   int32_t* sel = a.sel + q * a.k;
   uint2* cand = a.cand + q * kCandCap;
-  // uniform trip count so that the warp votes below see every lane; 4 keys per thread
-  const int64_t n_iter = (c1 - c0 + 4 * kTopkThreads - 1) / (4 * kTopkThreads);
-  for (int64_t it = 0; it < n_iter; ++it) {
-    const int64_t i0 = c0 + it * 4 * kTopkThreads + 4 * threadIdx.x;
-    uint32_t key[4], bin[4];
-    bool in[4];
-    if (i0 + 3 < c1) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(row + i0));
-      key[0] = order_key(v.x); key[1] = order_key(v.y); key[2] = order_key(v.z); key[3] = order_key(v.w);
-      in[0] = in[1] = in[2] = in[3] = true;
-    } else {
+  // all of this thread's loads go out together (16 keys per thread for a full chunk);
+  // the warp votes below see every lane
+  constexpr int kU = kChunk / (4 * kTopkThreads);
+  float4 v[kU];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        in[j] = i0 + j < c1;
-        key[j] = in[j] ? order_key(__ldg(row + i0 + j)) : 0u;
-      }
+  for (int u = 0; u < kU; ++u) {
+    const int64_t i0 = c0 + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
+    if (i0 + 3 < c1) {
+      v[u] = __ldg(reinterpret_cast<const float4*>(row + i0));
+    } else {
+      v[u].x = i0 + 0 < c1 ? __ldg(row + i0 + 0) : 0.0f;
+      v[u].y = i0 + 1 < c1 ? __ldg(row + i0 + 1) : 0.0f;
+      v[u].z = i0 + 2 < c1 ? __ldg(row + i0 + 2) : 0.0f;
+      v[u].w = i0 + 3 < c1 ? __ldg(row + i0 + 3) : 0.0f;
     }
-    bool any = false;
+  }
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    const int64_t i0 = c0 + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
+    const uint32_t key[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w)};
+    bool in[4], any = false;
+    uint32_t bin[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+      in[j] = i0 + j < c1;
       bin[j] = key[j] >> 21;
       any |= in[j] && bin[j] >= bstar;
     }
@@ -269,7 +279,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(const TopkArgs
   }
   for (uint32_t i = threadIdx.x; i < above; i += kTopkThreads) picked[i] = a.sel[q * a.k + i];
   __syncthreads();
-  if (nc <= kCandCap) {
+  if (nc <= 1024) {
+    // rank each candidate among all candidates by (key desc, index asc): no sort stages
+    const uint2* cand = a.cand + q * kCandCap;
+    for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
+      const uint2 c = cand[i];
+      cs[i] = (static_cast<uint64_t>(0xFFFFFFFFu - c.x) << 32) | c.y;
+    }
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
+      const uint64_t me = cs[i];
+      uint32_t rank = 0;
+      for (uint32_t j = 0; j < nc; ++j) rank += cs[j] < me;
+      if (rank < need) picked[above + rank] = static_cast<int32_t>(me & 0xFFFFFFFFu);
+    }
+    __syncthreads();
+  } else if (nc <= kCandCap) {
     int p2 = 1;
     while (p2 < static_cast<int>(nc)) p2 <<= 1;
     const uint2* cand = a.cand + q * kCandCap;
@@ -289,9 +314,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(const TopkArgs
     refine_row(a, q, nv, bstar, need, h, s_warp, picked, &n_picked);
     __syncthreads();
   }
-  // ascending order of the k chosen indices
-  bitonic_sort(picked, a.k);
-  for (int i = threadIdx.x; i < a.k; i += kTopkThreads) out[i] = picked[i];
+  // ascending order of the k chosen (distinct) indices: each index's rank is the number
+  // of smaller ones
+  for (int i = threadIdx.x; i < a.k; i += kTopkThreads) {
+    const int32_t me = picked[i];
+    int rank = 0;
+    for (int j = 0; j < a.k; ++j) rank += picked[j] < me;
+    out[rank] = me;
+  }
 }
 
 size_t topk_final_smem() { return kCandCap * sizeof(uint64_t) + kBins * sizeof(uint32_t) + 512 * sizeof(int32_t); }
