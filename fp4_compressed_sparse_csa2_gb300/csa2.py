@@ -22,7 +22,7 @@ TOPK, WIN, HEADS, PAGE = 512, 128, 64, 128
 KV_PAGE_BYTES, IDX_PAGE_BYTES = PAGE * KV_BYTES, PAGE * IDX_BYTES
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_DEVICE = range(7)
-TRACE_KINDS = {"pack": 0, "index": 1, "topk_hist": 2, "topk_select": 3, "topk_final": 4, "attn": 5}
+TRACE_KINDS = {"pack": 0, "index": 1, "topk_hist": 2, "topk_select": 3, "topk_final": 4, "attn": 5, "topk": 6}
 
 
 class Csa2Error(RuntimeError):

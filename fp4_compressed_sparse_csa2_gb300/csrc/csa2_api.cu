@@ -37,7 +37,7 @@ csa2_status cuda_fail(cudaError_t e, const char* what) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // ------------------------------------------------------------------ tracing
-enum Kind { kPack = 0, kIndex = 1, kTopkHist = 2, kTopkSel = 3, kTopkFinal = 4, kAttn = 5, kKinds = 6 };
+enum Kind { kPack = 0, kIndex = 1, kTopkHist = 2, kTopkSel = 3, kTopkFinal = 4, kAttn = 5, kTopk = 6, kKinds = 7 };
 constexpr int kTraceCap = 4096;
 
 struct Trace {
@@ -193,6 +193,25 @@ csa2_status run_topk(const float* scores, int64_t ld, const int32_t* n_visible, 
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "top-k kernels");
 }
 
+// One launch, one thread-block cluster per row (no scratch memory).
+csa2_status run_topk_cluster(const float* scores, int64_t ld, const int32_t* n_visible, int64_t n_q, int64_t t_max,
+                             int32_t k, int32_t* out, int32_t* err, cudaStream_t stream) {
+  if (n_q == 0) return CSA2_OK;
+  TopkArgs a{};
+  a.scores = scores;
+  a.ld = ld;
+  a.n_visible = n_visible;
+  a.n_q = n_q;
+  a.k = k;
+  a.out = out;
+  a.t_max = t_max;
+  a.err = err;
+  trace_begin(kTopk, stream);
+  const cudaError_t e = launch_topk_cluster(a, sm_count(), stream);
+  trace_end(kTopk, stream);
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "top-k kernel");
+}
+
 csa2_status run_attn(const csa2_step& s, int32_t* err, cudaStream_t stream) {
   if (s.n_q == 0) return CSA2_OK;
   AttnArgs a{};
@@ -266,7 +285,7 @@ csa2_status run_step(const csa2_step* s, Mode mode, void* ws, size_t ws_bytes, c
     st = run_index(s->cache, base + L.qpack, s->w, heads_I, s->req, s->n_visible, s->n_q, s->group, s->t_max, scores,
                    ld, err, stream);
     if (st != CSA2_OK) return st;
-    st = run_topk(scores, ld, s->n_visible, s->n_q, s->t_max, s->topk, s->topk_idx, base + L.topk, err, stream);
+    st = run_topk_cluster(scores, ld, s->n_visible, s->n_q, s->t_max, s->topk, s->topk_idx, err, stream);
     if (st != CSA2_OK) return st;
   }
   return run_attn(*s, err, stream);
@@ -330,8 +349,8 @@ csa2_status csa2_topk(const float* scores, int64_t ld, const int32_t* n_visible,
   const WsLayout L = ws_layout(n_q, 64, t_max, 0);
   csa2_status st = check_ws(ws, ws_bytes, L.total);
   if (st != CSA2_OK) return st;
-  return run_topk(scores, ld, n_visible, n_q, t_max, k, out_idx, static_cast<uint8_t*>(ws) + L.topk, err_word(ws),
-                  reinterpret_cast<cudaStream_t>(stream));
+  return run_topk_cluster(scores, ld, n_visible, n_q, t_max, k, out_idx, err_word(ws),
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 csa2_status csa2_sparse_attn_full(const csa2_step* step, void* ws, size_t ws_bytes, csa2_stream_t stream) {

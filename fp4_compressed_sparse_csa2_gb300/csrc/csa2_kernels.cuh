@@ -91,6 +91,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream, int kind_hist, i
 constexpr int64_t kStaticTopkRows = 128;
 constexpr int kMaxDevices = 64;
 cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes);
+cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream);
 size_t attn_smem_bytes();
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
 

@@ -11,8 +11,8 @@
 //            dequantise in registers (byte-permute lookups, exact bf16 products) and
 //            store the bf16 tile in the tensor-core operand layout; window rows are
 //            copied with cp.async;
-//   S^T      one thread issues 32 tcgen05.mma kind::f16 (M = 128 keys, N = 64 heads,
-//            K = 512) into TMEM;
+//   S^T      two threads issue 32 tcgen05.mma kind::f16 (M = 128 keys, N = 64 heads,
+//            K = 512) into four partial TMEM sums;
 //   softmax  thread = key, 32 heads per thread: warp max reductions, a per-head
 //            reference max that only moves when a tile exceeds it by 2^8 (then the
 //            TMEM accumulator and the running sums are rescaled), exp2, bf16 P^T to
@@ -49,9 +49,13 @@ __device__ __forceinline__ float redux_max(float v) {
   return r;
 }
 
+// E4M3 code -> bf16 (exact: 4 significant bits, range 2^-9 .. 448), both halves.
 __device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
-  const __nv_bfloat16 b = __float2bfloat16_rn(e4m3_value(code));
-  return __nv_bfloat162(b, b);
+  const uint32_t e = (code >> 3) & 15u, m = code & 7u;
+  uint32_t bits = e ? (((e + 120u) << 7) | (m << 4)) : (__float_as_uint(static_cast<float>(m) * 0.001953125f) >> 16);
+  bits |= (code & 0x80u) << 8;
+  const uint32_t both = bits | (bits << 16);
+  return *reinterpret_cast<const __nv_bfloat162*>(&both);
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a) {
@@ -66,9 +70,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   float* lred = tmax + 4 * kHeads;                        // [4][64]
   int64_t* recoff = reinterpret_cast<int64_t*>(lred + 4 * kHeads);     // [512] record byte offsets, -1 = none
   int32_t* tile_cnt = reinterpret_cast<int32_t*>(recoff + CSA2_TOPK);  // [4] valid entries per selected tile
-  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(tile_cnt + 4);
-  uint64_t* drain = mma_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(tile_cnt + 4);  // [2] one per MMA issuer
+  uint64_t* drain = mma_bar + 2;                                    // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   int32_t* flags = reinterpret_cast<int32_t*>(tmem_slot + 1);  // [0] abort, [1] rescale
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -77,8 +81,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   const int32_t wl = max(0, min(CSA2_WIN, __ldg(a.win_len + qi)));
 
   if (tid == 0) {
-    mbar_init(mma_bar, 1);
-    mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&mma_bar[i], 1);
+      mbar_init(&drain[i], 1);
+    }
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
@@ -176,14 +182,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     tc_fence_after();
 
     // ---------------------------------------------------------------- S^T = K Q^T
-    if (tid == 0) {
+    // two issuing threads (warps 0 and 1): issuer i takes K-steps kk = i, i+2, ... into
+    // partial sums i and i + 2, so neither thread waits on the other's MMA latency
+    if (lane == 0 && warp < 2) {
+      const uint32_t me = static_cast<uint32_t>(warp);
       const uint32_t kb = smem_u32(Kt), qb = smem_u32(Qs);
 #pragma unroll 4
-      for (uint32_t kk = 0; kk < 32; ++kk)  // kk % 4 picks one of four independent partial sums
+      for (uint32_t kk = me; kk < 32; kk += 2)
         mma_bf16(tmem + kSCols + (kk & 3u) * 64u, sdesc(kb + kk * 256u, 128, 8192), sdesc(qb + kk * 256u, 128, 8192),
                  idesc_s, kk >= 4 ? 1u : 0u);
-      mma_commit(mma_bar);
-      if (!mbar_wait(mma_bar, phase, nullptr)) {
+      mma_commit(&mma_bar[me]);
+      if (!mbar_wait(&mma_bar[me], phase, nullptr)) {
         flags[0] = 1;
         report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
       }
@@ -271,17 +280,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     tc_fence_after();
 
     // ---------------------------------------------------------------- O^T += V^T P^T
-    if (tid == 0) {
+    // issuer i accumulates output tiles 2i and 2i+1 (channels [256 i, 256 i + 256))
+    if (lane == 0 && warp < 2) {
+      const uint32_t me = static_cast<uint32_t>(warp);
       const uint32_t kb = smem_u32(Kt), pb = smem_u32(Ps);
       for (uint32_t kk = 0; kk < 8; ++kk) {
 #pragma unroll
-        for (uint32_t c = 0; c < 4; ++c) {  // four independent accumulators interleaved
+        for (uint32_t c = 2 * me; c < 2 * me + 2; ++c)
           mma_bf16(tmem + kOCols + c * 64u, sdesc(kb + c * 2048u + kk * 16384u, 8192, 128),
                    sdesc(pb + kk * 2048u, 1024, 128), idesc_o, (o_started || kk > 0) ? 1u : 0u);
-        }
       }
-      mma_commit(mma_bar);
-      if (!mbar_wait(mma_bar, phase, nullptr)) {
+      mma_commit(&mma_bar[me]);
+      if (!mbar_wait(&mma_bar[me], phase, nullptr)) {
         flags[0] = 1;
         report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
       }
@@ -310,7 +320,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       if (a.lse) a.lse[qi * kHeads + tid] = (l > 0.0f) ? (ref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();
-    __nv_bfloat16* og = a.out + qi * kHeads * CSA2_D;
+    // O^T (TMEM lane = channel, column = head) -> bf16 [64][512] staged in the free key
+    // tile, then written out with 16-byte coalesced stores
+    __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(Kt);
+    if (tid < kHeads) alpha[tid] = alpha[tid] > 0.0f ? 1.0f / alpha[tid] : 0.0f;  // 1 / row sum
+    __syncthreads();
     for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
       const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
       for (int h0 = 0; h0 < 64; h0 += 32) {
@@ -321,17 +335,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float l = alpha[h0 + i];
-          const float o = (o_started && l > 0.0f) ? __uint_as_float(r[i]) / l : 0.0f;
-          og[static_cast<int64_t>(h0 + i) * CSA2_D + d] = __float2bfloat16_rn(o);
+          const float o = o_started ? __uint_as_float(r[i]) * alpha[h0 + i] : 0.0f;
+          ostage[(h0 + i) * CSA2_D + d] = __float2bfloat16_rn(o);
         }
       }
     }
+    __syncthreads();
+    uint4* og = reinterpret_cast<uint4*>(a.out + qi * kHeads * CSA2_D);
+    const uint4* os = reinterpret_cast<const uint4*>(ostage);
+    for (int i = tid; i < kHeads * CSA2_D / 8; i += kAttnThreads) og[i] = os[i];
   }
   // drain outstanding MMAs, then free TMEM
-  if (tid == 0) {
-    mma_commit(drain);
-    mbar_wait(drain, 0, nullptr);
+  if (lane == 0 && warp < 2) {
+    mma_commit(&drain[warp]);
+    mbar_wait(&drain[warp], 0, nullptr);
   }
   tc_fence_before();
   __syncthreads();
@@ -340,7 +357,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
 }
 
 size_t attn_smem_bytes() {
-  return 1024 + kKtBytes + kQsBytes + kPsBytes + (2 + 8) * kHeads * sizeof(float) + 64 + CSA2_TOPK * 8 + 16;
+  return 1024 + kKtBytes + kQsBytes + kPsBytes + (2 + 8) * kHeads * sizeof(float) + 80 + CSA2_TOPK * 8 + 16;
 }
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {

@@ -398,3 +398,252 @@ cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes) {
 }
 
 }  // namespace csa2
+
+// ----------------------------------------------------------------------------
+// Cluster top-k: one launch, one thread-block cluster of C CTAs per score row.
+// Each CTA histograms its chunk; the cluster sums the histograms through distributed
+// shared memory; each CTA re-reads its chunk and appends the indices above the
+// threshold bin and the candidates inside it to the leader CTA's shared memory; the
+// leader resolves the threshold bin exactly and writes the row.  No workspace, no
+// polling: the only waits are hardware cluster barriers.
+namespace csa2 {
+
+constexpr int kClCandCap = 8192;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t dsmem_map(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_st2(uint32_t addr, uint32_t x, uint32_t y) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Warp-aggregated append to a counter in the leader's shared memory.
+__device__ __forceinline__ uint32_t dsmem_append(uint32_t counter, bool pred) {
+  const uint32_t m = __ballot_sync(0xffffffffu, pred);
+  if (m == 0) return 0;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = dsmem_atom_add(counter, static_cast<uint32_t>(__popc(m)));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(m & ((1u << lane) - 1u));
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkArgs a, int64_t chunk) {
+  extern __shared__ __align__(16) uint8_t tc_smem[];
+  uint32_t* h = reinterpret_cast<uint32_t*>(tc_smem);   // [kBins] this CTA's histogram
+  uint32_t* hsum = h + kBins;                           // [kBins] row histogram
+  uint32_t* ctr = hsum + kBins;                         // [4] leader: selected, candidates, picked
+  int32_t* sel = reinterpret_cast<int32_t*>(ctr + 4);   // [512] leader: chosen indices
+  uint2* cand = reinterpret_cast<uint2*>(sel + 512);    // [kClCandCap] leader: (key, index)
+  __shared__ uint32_t s_warp[32];
+  __shared__ int s_bin;
+  __shared__ uint32_t s_above;
+  const uint32_t rank = cluster_rank();
+  const uint32_t csize = gridDim.x;  // one cluster spans the x dimension
+  const int64_t q = blockIdx.y;
+  const int64_t nv = row_visible(a, q);
+  int32_t* out = a.out + q * a.k;
+  if (nv <= a.k) {  // the whole row is selected (uniform across the cluster)
+    if (rank == 0)
+      for (int i = threadIdx.x; i < a.k; i += kTopkThreads) out[i] = i < nv ? i : -1;
+    return;
+  }
+  const int64_t c0 = static_cast<int64_t>(rank) * chunk;
+  const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
+  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
+  if (threadIdx.x < 4) ctr[threadIdx.x] = 0;
+  __syncthreads();
+  const float* row = a.scores + q * a.ld;
+  // ---- pass 1: histogram of the top 11 key bits (4 float4 per thread in flight)
+  for (int64_t base = c0; base < c1; base += 16 * kTopkThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
+      if (i0 + 3 < c1) {
+        v[u] = __ldg(reinterpret_cast<const float4*>(row + i0));
+      } else {
+        v[u].x = i0 + 0 < c1 ? __ldg(row + i0 + 0) : NAN;
+        v[u].y = i0 + 1 < c1 ? __ldg(row + i0 + 1) : NAN;
+        v[u].z = i0 + 2 < c1 ? __ldg(row + i0 + 2) : NAN;
+        v[u].w = i0 + 3 < c1 ? __ldg(row + i0 + 3) : NAN;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
+      if (i0 + 0 < c1) atomicAdd(&h[order_key(v[u].x) >> 21], 1u);
+      if (i0 + 1 < c1) atomicAdd(&h[order_key(v[u].y) >> 21], 1u);
+      if (i0 + 2 < c1) atomicAdd(&h[order_key(v[u].z) >> 21], 1u);
+      if (i0 + 3 < c1) atomicAdd(&h[order_key(v[u].w) >> 21], 1u);
+    }
+  }
+  cluster_sync_all();  // every CTA's histogram and the leader's counters are ready
+  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
+    uint32_t sum = 0;
+    for (uint32_t r = 0; r < csize; ++r) sum += dsmem_ld(dsmem_map(&h[b], r));
+    hsum[b] = sum;
+  }
+  __syncthreads();
+  threshold_bin(hsum, static_cast<uint32_t>(a.k), &s_bin, &s_above, s_warp);
+  const uint32_t bstar = static_cast<uint32_t>(s_bin);
+  // ---- pass 2: append to the leader (the chunk is mostly still in L2)
+  const uint32_t l_ctr = dsmem_map(&ctr[0], 0), l_sel = dsmem_map(sel, 0), l_cand = dsmem_map(cand, 0);
+  for (int64_t base = c0; base < c1; base += 16 * kTopkThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
+      if (i0 + 3 < c1) {
+        v[u] = __ldg(reinterpret_cast<const float4*>(row + i0));
+      } else {
+        v[u].x = i0 + 0 < c1 ? __ldg(row + i0 + 0) : 0.0f;
+        v[u].y = i0 + 1 < c1 ? __ldg(row + i0 + 1) : 0.0f;
+        v[u].z = i0 + 2 < c1 ? __ldg(row + i0 + 2) : 0.0f;
+        v[u].w = i0 + 3 < c1 ? __ldg(row + i0 + 3) : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
+      const uint32_t key[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w)};
+      bool any = false;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) any |= (i0 + j < c1) && (key[j] >> 21) >= bstar;
+      if (!__any_sync(0xffffffffu, any)) continue;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool in = i0 + j < c1;
+        const uint32_t bin = key[j] >> 21;
+        const bool hi = in && bin > bstar;
+        uint32_t slot = dsmem_append(l_ctr, hi);
+        if (hi && slot < static_cast<uint32_t>(a.k)) dsmem_st(l_sel + 4u * slot, static_cast<uint32_t>(i0 + j));
+        const bool eq = in && bin == bstar;
+        slot = dsmem_append(l_ctr + 4u, eq);
+        if (eq && slot < kClCandCap) dsmem_st2(l_cand + 8u * slot, key[j], static_cast<uint32_t>(i0 + j));
+      }
+    }
+  }
+  cluster_sync_all();  // every append has landed in the leader
+  if (rank != 0) return;
+  // ---- leader: resolve the threshold bin exactly
+  const uint32_t above = s_above, nc = hsum[bstar], need = static_cast<uint32_t>(a.k) - above;
+  if (threadIdx.x == 0) {
+    if (ctr[0] != above || ctr[1] != nc) report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
+    ctr[2] = above;
+  }
+  __syncthreads();
+  uint32_t* hA = h;  // reuse this CTA's histogram as scratch
+  bool done = false;
+  if (nc <= kClCandCap) {
+    // level A: bits [10, 21) below the 11-bit prefix
+    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) hA[b] = 0;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) atomicAdd(&hA[(cand[i].x >> 10) & 0x7FFu], 1u);
+    __syncthreads();
+    threshold_bin(hA, need, &s_bin, &s_above, s_warp);
+    const uint32_t binA = static_cast<uint32_t>(s_bin), needA = need - s_above;
+    __syncthreads();
+    // level B: bits [0, 10) among the candidates of sub-bin binA
+    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) hA[b] = 0;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
+      const uint32_t key = cand[i].x;
+      if (((key >> 10) & 0x7FFu) == binA) atomicAdd(&hA[key & 0x3FFu], 1u);
+    }
+    __syncthreads();
+    threshold_bin(hA, needA, &s_bin, &s_above, s_warp);
+    const uint32_t binB = static_cast<uint32_t>(s_bin), needB = needA - s_above;
+    const uint32_t vstar = (bstar << 21) | (binA << 10) | binB;
+    const uint32_t n_ties = hA[binB];
+    __syncthreads();
+    if (n_ties <= kBins) {
+      // keys above vstar are chosen; ties at vstar are collected and the lowest indices taken
+      int32_t* ties = reinterpret_cast<int32_t*>(hsum);
+      if (threadIdx.x == 0) ctr[3] = 0;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
+        const uint2 c = cand[i];
+        if (c.x > vstar) sel[atomicAdd(&ctr[2], 1u)] = static_cast<int32_t>(c.y);
+        else if (c.x == vstar) ties[atomicAdd(&ctr[3], 1u)] = static_cast<int32_t>(c.y);
+      }
+      __syncthreads();
+      int p2 = 1;
+      while (p2 < static_cast<int>(n_ties)) p2 <<= 1;
+      for (int i = static_cast<int>(n_ties) + threadIdx.x; i < p2; i += kTopkThreads) ties[i] = 0x7FFFFFFF;
+      __syncthreads();
+      bitonic_sort(ties, p2);
+      const uint32_t base = above + (need - needB);
+      for (uint32_t i = threadIdx.x; i < needB; i += kTopkThreads) sel[base + i] = ties[i];
+      __syncthreads();
+      done = true;
+    }
+  }
+  if (!done) {
+    // massive ties: exact radix refinement over the whole row
+    refine_row(a, q, nv, bstar, need, h, s_warp, sel, &ctr[2]);
+    __syncthreads();
+  }
+  bitonic_sort(sel, a.k);
+  for (int i = threadIdx.x; i < a.k; i += kTopkThreads) out[i] = sel[i];
+}
+
+size_t topk_cluster_smem() {
+  return 2 * kBins * sizeof(uint32_t) + 4 * sizeof(uint32_t) + 512 * sizeof(int32_t) + kClCandCap * sizeof(uint2);
+}
+
+cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream) {
+  if (a.n_q == 0) return cudaSuccess;
+  // cluster size: enough CTAs to fill the GPU about twice, at most 8 (portable), and
+  // chunks of at least 8K entries
+  int64_t c = (2 * static_cast<int64_t>(sm_count) + a.n_q - 1) / a.n_q;
+  const int64_t by_len = (a.t_max + 8191) / 8192;
+  if (c > by_len) c = by_len;
+  if (c < 1) c = 1;
+  if (c > 8) c = 8;
+  int64_t chunk = (a.t_max + c - 1) / c;
+  chunk = ((chunk + 2047) / 2048) * 2048;
+  const size_t smem = topk_cluster_smem();
+  cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c), static_cast<unsigned>(a.n_q), 1);
+  cfg.blockDim = dim3(kTopkThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a, chunk);
+}
+
+}  // namespace csa2
