@@ -15,9 +15,11 @@ the slowest rank's time is reported.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import concurrent.futures as cf
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -46,6 +48,7 @@ def parse():
     p.add_argument("--ctx", type=int, default=131072, help="cached entries per request (the workload uses 131072)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before timing (clock sampling)")
     return p.parse_args()
 
 
@@ -247,6 +250,25 @@ def oracle_sample(wl: "Workload", n_req: int, threads: int):
     return time.perf_counter() - t0, len(reqs)
 
 
+def profiled_traffic(summary: str, sources, entries: int):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, scaled by entries scored;
+    None when the kernel's sources no longer hash to the captured ones."""
+    try:
+        text = open(os.path.join(ROOT, "profiles", summary)).read()
+    except OSError:
+        return None
+    m = hashlib.sha256()
+    for f in sources:
+        m.update(open(os.path.join(ROOT, "fp4_compressed_sparse_csa2_gb300", "csrc", f), "rb").read())
+    fields = dict(re.findall(r"^(source_sha256|captured_entries): (\S+)", text, re.M))
+    rd = re.search(r"dram__bytes_read\.sum \| ([0-9.]+) MB", text)
+    wr = re.search(r"dram__bytes_write\.sum \| ([0-9.]+) MB", text)
+    if fields.get("source_sha256") != m.hexdigest() or not rd or not wr:
+        return None
+    per_entry = (float(rd.group(1)) + float(wr.group(1))) * 1e6 / int(fields["captured_entries"])
+    return int(round(per_entry * entries))
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -267,7 +289,7 @@ def run_ours(args, ws, rank, local):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         # untimed soak so that the sampler (200 ms period) sees the GPU under this load
-        t_end = time.time() + 1.5
+        t_end = time.time() + args.soak
         while time.time() < t_end:
             for _ in range(20):
                 wl.run()
@@ -298,6 +320,8 @@ def run_ours(args, ws, rank, local):
     # roofline of the dominant kernel (the indexer): algorithmic bytes = 72 B per scored entry
     idx_us = kernels["index"]["us_per_launch"]
     idx_bytes = wl.B * wl.T * 72
+    traffic = profiled_traffic("index_kernel_decode_b16_t131072.md", ("k_index.cu", "csa2_dev.cuh", "csa2_kernels.cuh"),
+                               wl.B * wl.T)
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -308,7 +332,9 @@ def run_ours(args, ws, rank, local):
     roofline = {"bound": "hbm", "kernel": "index_kernel", "achieved": round(achieved, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks else "fallback 6.8 TB/s",
-                "traffic": None, "algorithmic_bytes": idx_bytes}
+                "traffic": traffic, "algorithmic_bytes": idx_bytes,
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of a 16-request capture, scaled "
+                                  "by entries scored (null once the kernel source differs from the capture's)"}
     step_gbs = wl.must_read_bytes() / (ms * 1e-3) / 1e9
 
     # end to end through the C ABI with host buffers
@@ -363,7 +389,8 @@ def run_ours(args, ws, rank, local):
             "data": "synthetic (seeded N(0,1) latents, keys, queries; fp32 N(0,1) head weights)",
             "config": {"workload": workload_name(wl.B, wl.T), "global_batch": wl.B * ws, "seq_len": wl.T,
                        "parallelism": f"replicas x{ws} (requests sharded, no collective)",
-                       "l2": "inputs larger than L2: 604 MB of indexer keys per step stream from HBM"},
+                       "l2": f"inputs larger than L2: {wl.B * wl.T * 72 / 1e6:.0f} MB of indexer keys per step "
+                             f"stream from HBM"},
             "hbm": {"must_read_bytes_per_step": wl.must_read_bytes(), "step_gbs": round(step_gbs, 1),
                     "frac_of_8tbs": round(step_gbs / NOMINAL_HBM_GBS, 4),
                     "frac_of_measured": round(step_gbs / hbm_peak, 4)},
