@@ -15,6 +15,21 @@
 
 using namespace csa2;
 
+namespace csa2 {
+
+cudaError_t smem_limit_once(const void* kernel, size_t bytes, std::atomic<int>* cache) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && cache[dev].load(std::memory_order_acquire) >= static_cast<int>(bytes)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && cached) cache[dev].store(static_cast<int>(bytes), std::memory_order_release);
+  return e;
+}
+
+}  // namespace csa2
+
 namespace {
 
 thread_local std::string g_last_error;

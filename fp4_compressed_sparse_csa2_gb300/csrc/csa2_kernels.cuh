@@ -3,6 +3,8 @@
 
 #include "csa2_dev.cuh"
 
+#include <atomic>
+
 namespace csa2 {
 
 struct PackArgs {
@@ -90,6 +92,11 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream, int kind_hist, i
 // current device (looked up on first use per device).
 constexpr int64_t kStaticTopkRows = 128;
 constexpr int kMaxDevices = 64;
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` once per device; `cache` holds
+// kMaxDevices entries of the limit already set.  cudaFuncSetAttribute on every launch
+// leaves the GPU idle between back-to-back launches.
+cudaError_t smem_limit_once(const void* kernel, size_t bytes, std::atomic<int>* cache);
 cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes);
 cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream);
 size_t attn_smem_bytes();

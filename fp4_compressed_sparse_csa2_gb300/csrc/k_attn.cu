@@ -363,8 +363,8 @@ size_t attn_smem_bytes() {
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_q == 0) return cudaSuccess;
   const size_t smem = attn_smem_bytes();
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static std::atomic<int> limit_set[kMaxDevices];
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(attn_kernel), smem, limit_set);
   if (e != cudaSuccess) return e;
   attn_kernel<<<static_cast<unsigned>(a.n_q), kAttnThreads, smem, stream>>>(a);
   return cudaGetLastError();

@@ -26,7 +26,8 @@ namespace csa2 {
 constexpr uint32_t kIssuers = 4;    // MMA-issuing warps
 constexpr uint32_t kEpiGroups = 4;  // epilogue warpgroups
 constexpr int kIdxThreads = 32 * (1 + kIssuers + 4 * kEpiGroups);  // producer, issuers, epilogue
-constexpr int kIdxStages = 16;  // ring capacity in pages (147 KB); a stage holds n_iss pages
+constexpr int kLgStages = 4;
+constexpr int kIdxStages = 1 << kLgStages;  // ring capacity in pages (147 KB); a stage holds n_iss pages
 constexpr float kInvSqrtDI = 0.08838834764831845f;  // 128^-0.5
 
 // The CTA's range [begin, end) of the flat (group, tile) space, walked as group
@@ -127,70 +128,77 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
   const int64_t g_last = end > begin ? (end - 1) / a.tpg : g_first - 1;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      // Stage k holds the pages of tiles k*n_iss .. k*n_iss + n_iss - 1 (one per issuer);
-      // pages adjacent in memory go in one bulk copy.
-      const uint64_t pol = policy_evict_first();
-      const uint32_t n_st = kIdxStages / n_iss;
-      uint32_t k = 0, ph = 0, in_st = 0, n_stages = 0, m = 0, run_len = 0;
-      int64_t run_page = 0;
-      uint8_t* run_dst = ring;
-      bool ok = true;
-      auto flush = [&]() {
-        if (run_len) {
-          const uint32_t bytes = run_len * static_cast<uint32_t>(kIdxPageBytes);
-          mbar_expect_tx(&full[k], bytes);
-          bulk_g2s_hint(run_dst, a.idx_pages + run_page * kIdxPageBytes, bytes, &full[k], pol);
-          run_len = 0;
-        }
-      };
-      Segment sg;
-      for (int64_t g = g_first; ok && g <= g_last; ++g) {
-        if (!segment(a, g, begin, end, sg)) continue;
-        {
-          const uint32_t slot = m & 1u;
-          ok = mbar_wait(&q_empty[slot], ((m >> 1) & 1u) ^ 1u, abort);
-          if (!ok) break;
+    // -------------------------------------------------------------- producer (one warp)
+    // Stage k holds the pages of CTA-local tiles k*n_iss .. k*n_iss + n_iss - 1 (one per
+    // issuer).  Without a block table a request's pages are adjacent, so lane 0 moves a
+    // stage's pages of one group with a single bulk copy; with a block table each lane
+    // looks up and copies one page, so the lookups overlap.  The per-stage work of this
+    // warp is kept to a few dozen instructions: it bounds the rate at which the ring refills.
+    const uint64_t pol = policy_evict_first();
+    const uint32_t n_st = kIdxStages / n_iss;
+    uint32_t k = 0, ph = 0, n = 0, n_stages = 0, m = 0;
+    bool ok = true;
+    Segment sg;
+    for (int64_t g = g_first; ok && g <= g_last; ++g) {
+      if (!segment(a, g, begin, end, sg)) continue;
+      if (lane == 0) {
+        const uint32_t slot = m & 1u;
+        ok = mbar_wait(&q_empty[slot], ((m >> 1) & 1u) ^ 1u, abort);
+        if (ok) {
           mbar_arrive_expect_tx(&q_full[slot], static_cast<uint32_t>(a.grp_bytes));
           bulk_g2s(qslot + slot * kIdxPageBytes, a.qpack + g * a.grp_bytes, static_cast<uint32_t>(a.grp_bytes),
                    &q_full[slot]);
-          ++m;
         }
-        for (int32_t t = sg.t0; t < sg.t1; ++t) {
-          if (in_st == 0) {
-            ok = mbar_wait(&empty[k], ph ^ 1u, abort);
-            if (!ok) break;
-          }
-          const int64_t page = seg_page(sg, t);
-          uint8_t* dst = ring + (k * n_iss + in_st) * kIdxPageBytes;
-          if (page >= 0 && page < a.cache.n_pages) {
-            if (run_len && page == run_page + run_len) {
-              ++run_len;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++m;
+      for (int32_t t = sg.t0; t < sg.t1;) {
+        const uint32_t in_st = n & (n_iss - 1u);
+        const int32_t left = sg.t1 - t;
+        const int32_t cnt = left < static_cast<int32_t>(n_iss - in_st) ? left : static_cast<int32_t>(n_iss - in_st);
+        if (in_st == 0) {
+          if (lane == 0) ok = mbar_wait(&empty[k], ph ^ 1u, abort);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+        uint8_t* dst = ring + (k * n_iss + in_st) * kIdxPageBytes;
+        if (sg.bt_row == nullptr) {
+          if (lane == 0) {
+            const int64_t page = sg.page_base + t;
+            if (page >= 0 && page + cnt <= a.cache.n_pages) {
+              const uint32_t bytes = static_cast<uint32_t>(cnt) * static_cast<uint32_t>(kIdxPageBytes);
+              mbar_expect_tx(&full[k], bytes);
+              bulk_g2s_hint(dst, a.idx_pages + page * kIdxPageBytes, bytes, &full[k], pol);
             } else {
-              flush();
-              run_page = page;
-              run_len = 1;
-              run_dst = dst;
+              report(a.err, CSA2_ERR_DEVICE, kInfoPage);
             }
+          }
+        } else if (lane < cnt) {
+          const int64_t page = __ldg(sg.bt_row + t + lane);
+          if (page >= 0 && page < a.cache.n_pages) {
+            mbar_expect_tx(&full[k], static_cast<uint32_t>(kIdxPageBytes));
+            bulk_g2s_hint(dst + lane * kIdxPageBytes, a.idx_pages + page * kIdxPageBytes,
+                          static_cast<uint32_t>(kIdxPageBytes), &full[k], pol);
           } else {
-            flush();
             report(a.err, CSA2_ERR_DEVICE, kInfoPage);
           }
-          if (++in_st == n_iss) {
-            flush();
-            mbar_arrive(&full[k]);
-            in_st = 0;
-            ++n_stages;
-            if (++k == n_st) {
-              k = 0;
-              ph ^= 1u;
-            }
+        }
+        __syncwarp();
+        t += cnt;
+        n += static_cast<uint32_t>(cnt);
+        if ((n & (n_iss - 1u)) == 0) {
+          if (lane == 0) mbar_arrive(&full[k]);
+          ++n_stages;
+          if (++k == n_st) {
+            k = 0;
+            ph ^= 1u;
           }
         }
       }
-      if (ok && in_st) {  // partial last stage
-        flush();
+    }
+    if (lane == 0) {
+      if (ok && (n & (n_iss - 1u))) {  // partial last stage
         mbar_arrive(&full[k]);
         ++n_stages;
       }
@@ -211,6 +219,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
       // the copy ring moving
       const uint32_t me = static_cast<uint32_t>(warp - 1);
       const uint32_t idesc = idesc_nvf4(128, a.N);
+      const uint32_t lg_iss = n_iss == 4u ? 2u : (n_iss == 2u ? 1u : 0u);
+      const uint32_t lg_st = kLgStages - lg_iss, lg_acc = n_acc == 4 ? 2u : 1u;
       uint32_t n = 0, m = 0, cur = 0;
       bool ok = true;
       Segment sg;
@@ -226,11 +236,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         tmem_cp_sf(sfb, sdesc(qs + nib_q, 128, 128));
         tmem_cp_sf(sfb + 4, sdesc(qs + nib_q + 512, 128, 128));
         ++m;
-        for (int32_t t = sg.t0; t < sg.t1; ++t, ++n) {
-          if ((n & (n_iss - 1)) != me) continue;
-          const uint32_t kst = n / n_iss, n_st = kIdxStages / n_iss;
-          const uint32_t s = kst % n_st, ph = (kst / n_st) & 1u;
-          const uint32_t b = n & static_cast<uint32_t>(n_acc - 1), bph = (n >> (n_acc == 4 ? 2 : 1)) & 1u;
+        // CTA-local tiles n .. n + len - 1 belong to this segment; this issuer's are the
+        // ones with nn % n_iss == me
+        const uint32_t len = static_cast<uint32_t>(sg.t1 - sg.t0);
+        for (uint32_t nn = n + ((me - n) & (n_iss - 1u)); nn < n + len; nn += n_iss) {
+          const uint32_t kst = nn >> lg_iss;
+          const uint32_t s = kst & ((1u << lg_st) - 1u), ph = (kst >> lg_st) & 1u;
+          const uint32_t b = nn & static_cast<uint32_t>(n_acc - 1), bph = (nn >> lg_acc) & 1u;
           ok = mbar_wait(&full[s], ph, abort);
           if (!ok) break;
           ok = mbar_wait(&acc_empty[b], bph ^ 1u, abort);
@@ -247,6 +259,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
           mma_commit(&empty[s]);
           mma_commit(&acc_full[b]);
         }
+        n += len;
       }
       if (!ok) {
         *abort = 1;
@@ -280,10 +293,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
       }
       __syncwarp();
       const int nq = static_cast<int>(a.n_q - q0 < a.G ? a.n_q - q0 : a.G);
-      for (int32_t t = sg.t0; t < sg.t1; ++t, ++n) {
-        if ((n & (n_wg - 1)) != wg) continue;
-        const uint32_t bb = n & static_cast<uint32_t>(n_acc - 1);
-        const uint32_t bp = (n >> (n_acc == 4 ? 2 : 1)) & 1u;
+      const uint32_t len = static_cast<uint32_t>(sg.t1 - sg.t0);
+      for (uint32_t nn = n + ((wg - n) & (n_wg - 1u)); nn < n + len; nn += n_wg) {
+        const int32_t t = sg.t0 + static_cast<int32_t>(nn - n);
+        const uint32_t bb = nn & static_cast<uint32_t>(n_acc - 1);
+        const uint32_t bp = (nn >> (n_acc == 4 ? 2 : 1)) & 1u;
         const int64_t page = seg_page(sg, t);
         const bool page_ok = page >= 0 && page < a.cache.n_pages;
         volatile int32_t* my_go = go + 2 * wg + (own & 1u);
@@ -321,6 +335,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         tc_fence_before();
         mbar_arrive(&acc_empty[bb]);
       }
+      n += len;
     }
     if (!ok) {
       *abort = 1;
@@ -341,8 +356,8 @@ size_t index_smem_bytes(int stages) {
 
 cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream) {
   const size_t smem = index_smem_bytes(a.stages);
-  cudaError_t e = cudaFuncSetAttribute(index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static std::atomic<int> limit_set[kMaxDevices];
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(index_kernel), smem, limit_set);
   if (e != cudaSuccess) return e;
   index_kernel<<<grid, kIdxThreads, smem, stream>>>(a);
   return cudaGetLastError();

@@ -357,7 +357,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream, int kind_hist, i
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const size_t smem = topk_final_smem();
-  e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static std::atomic<int> limit_set[kMaxDevices];
+  e = smem_limit_once(reinterpret_cast<const void*>(topk_final_kernel), smem, limit_set);
   if (e != cudaSuccess) return e;
   trace_begin(kind_final, stream);
   topk_final_kernel<<<static_cast<unsigned>(a.n_q), kTopkThreads, smem, stream>>>(a);
@@ -628,8 +629,8 @@ cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t st
   int64_t chunk = (a.t_max + c - 1) / c;
   chunk = ((chunk + 2047) / 2048) * 2048;
   const size_t smem = topk_cluster_smem();
-  cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static std::atomic<int> limit_set[kMaxDevices];
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(topk_cluster_kernel), smem, limit_set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c), static_cast<unsigned>(a.n_q), 1);
