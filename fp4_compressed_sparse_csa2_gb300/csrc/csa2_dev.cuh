@@ -229,6 +229,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+// acc += w * x on two fp32 lanes with one packed FMA (round to nearest per lane).
+__device__ __forceinline__ void fma2(float2& acc, float2 w, float2 x) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long*>(&w)), "l"(*reinterpret_cast<unsigned long long*>(&x)),
+        "l"(*reinterpret_cast<unsigned long long*>(&acc)));
+  acc = *reinterpret_cast<float2*>(&d);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"

@@ -8,18 +8,22 @@
 //
 // Design: one persistent CTA per SM (21 warps) over a contiguous range of 128-key
 // tiles (one indexer page each):
-//   warp 0      producer: one 9216-byte bulk copy per page (the page is stored in the
-//               MMA's operand layout) and one per packed query group, into a
-//               16-deep mbarrier ring (147 KB in flight per SM);
-//   warps 1-4   TMEM allocator (warp 1) and four MMA issuers: tcgen05.cp of the E4M3 scale atoms,
-//               then two tcgen05.mma kind::mxf4nvf4 (K = 64 each) per tile into one of
-//               4 (N <= 64) or 2 (N = 128) fp32 TMEM accumulators D[128 keys][N];
+//   warp 0      producer: a 16-page mbarrier ring of bulk copies (147 KB in flight per
+//               SM; the page is stored in the MMA's operand layout), one copy per stage of
+//               adjacent pages, plus one per packed query group;
+//   warps 1-4   TMEM allocator (warp 1) and four MMA issuers: tcgen05.cp of the E4M3 scale
+//               atoms into double-buffered TMEM slots as soon as a page lands, then, once
+//               the accumulator is free, two tcgen05.mma kind::mxf4nvf4 (K = 64 each) into
+//               one of 4 (N <= 64) or 2 (N = 128) fp32 TMEM accumulators D[128 keys][N];
 //   warps 5..20 four epilogue warpgroups taking every fourth tile: tcgen05.ld of one TMEM
-//               row per thread (thread = key), ReLU, head weights, head sum with four
-//               independent accumulators, x 128^-0.5, coalesced fp32 stores.
+//               row per thread (thread = key), 32 columns at a time; the accumulator goes
+//               back to its issuer as soon as the last columns are in registers.  ReLU,
+//               head weights and head sum use packed fp32x2 FMAs over four partial sums,
+//               then x 128^-0.5 and coalesced fp32 stores.
 // Every wait is bounded; a timeout sets the workspace error word, and the CTA drains
 // its copies and MMAs, frees TMEM and returns.
 #include "csa2_kernels.cuh"
+
 
 namespace csa2 {
 
@@ -232,7 +236,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         if (!ok) break;
         tc_fence_after();
         const uint32_t qs = smem_u32(qslot + cur * kIdxPageBytes);
-        const uint32_t sfb = tmem + 288u + 16u * me + 8u * cur;  // 288..351
+        const uint32_t sfb = tmem + 320u + 16u * me + 8u * cur;  // 320..383
         tmem_cp_sf(sfb, sdesc(qs + nib_q, 128, 128));
         tmem_cp_sf(sfb + 4, sdesc(qs + nib_q + 512, 128, 128));
         ++m;
@@ -245,13 +249,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
           const uint32_t b = nn & static_cast<uint32_t>(n_acc - 1), bph = (nn >> lg_acc) & 1u;
           ok = mbar_wait(&full[s], ph, abort);
           if (!ok) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(ring + (s * n_iss + me) * kIdxPageBytes);
+          const uint32_t sfa = tmem + 256u + 16u * b + 8u * bph;  // 256..319
+          tmem_cp_sf(sfa, sdesc(st + kIdxNibBytes, 128, 128));
+          tmem_cp_sf(sfa + 4, sdesc(st + kIdxNibBytes + 512, 128, 128));
           ok = mbar_wait(&acc_empty[b], bph ^ 1u, abort);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t st = smem_u32(ring + (s * n_iss + me) * kIdxPageBytes);
-          const uint32_t sfa = tmem + 256u + 8u * b;
-          tmem_cp_sf(sfa, sdesc(st + kIdxNibBytes, 128, 128));
-          tmem_cp_sf(sfa + 4, sdesc(st + kIdxNibBytes + 512, 128, 128));
 #pragma unroll
           for (uint32_t kk = 0; kk < 2; ++kk)
             mma_nvf4(tmem + b * N, sdesc(st + kk * 256u, 128, 512), sdesc(qs + kk * 256u, 128, 512), idesc,
@@ -313,27 +318,33 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         }
         tc_fence_after();
         const int32_t key = t * kPage + static_cast<int32_t>(row);
-        for (int gq = 0; gq < nq; ++gq) {
-          float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
-          for (int c0 = 0; c0 < a.heads_I; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + bb * N + static_cast<uint32_t>(gq * a.heads_I + c0), r);
-            tmem_ld_wait();
-            const float4* w4 = reinterpret_cast<const float4*>(sw + gq * a.heads_I + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 wv = w4[i];
-              acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * i + 0]), 0.0f), acc0);
-              acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * i + 1]), 0.0f), acc1);
-              acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * i + 2]), 0.0f), acc2);
-              acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * i + 3]), 0.0f), acc3);
-            }
+        const uint32_t hmask = static_cast<uint32_t>(a.heads_I) - 1u;
+        const uint32_t lg_h = a.heads_I == 64 ? 6u : 5u;
+        float2 acc01 = make_float2(0.0f, 0.0f), acc23 = make_float2(0.0f, 0.0f);
+        for (uint32_t c = 0; c < N; c += 32u) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + bb * N + c, r);
+          tmem_ld_wait();
+          if (c + 32u >= N) {
+            tc_fence_before();
+            mbar_arrive(&acc_empty[bb]);
           }
-          if (page_ok && key < (gq == 0 ? sg.nv0 : sg.nv1))
-            a.scores[(q0 + gq) * a.ld + key] = ((acc0 + acc1) + (acc2 + acc3)) * kInvSqrtDI;
+          const float4* w4 = reinterpret_cast<const float4*>(sw + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 wv = w4[i];
+            fma2(acc01, make_float2(wv.x, wv.y),
+                 make_float2(fmaxf(__uint_as_float(r[4 * i + 0]), 0.0f), fmaxf(__uint_as_float(r[4 * i + 1]), 0.0f)));
+            fma2(acc23, make_float2(wv.z, wv.w),
+                 make_float2(fmaxf(__uint_as_float(r[4 * i + 2]), 0.0f), fmaxf(__uint_as_float(r[4 * i + 3]), 0.0f)));
+          }
+          if (((c + 32u) & hmask) == 0) {
+            const int gq = static_cast<int>(c >> lg_h);
+            if (gq < nq && page_ok && key < (gq == 0 ? sg.nv0 : sg.nv1))
+              a.scores[(q0 + gq) * a.ld + key] = ((acc01.x + acc01.y) + (acc23.x + acc23.y)) * kInvSqrtDI;
+            acc01 = acc23 = make_float2(0.0f, 0.0f);
+          }
         }
-        tc_fence_before();
-        mbar_arrive(&acc_empty[bb]);
       }
       n += len;
     }
