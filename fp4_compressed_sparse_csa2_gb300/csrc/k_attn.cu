@@ -6,18 +6,21 @@
 // the FP4 entries are dequantised before attention.  "From MLA to DSA to HCA/CSA",
 // "What replaced MLA": attention(q, kv, kv) with K and V the same tensor.
 //
-// Design (one CTA of 8 warps per query; 64 heads; 5 key tiles of 128 keys):
-//   build    all warps gather 128 entries (16-byte loads of the 288-byte records),
-//            dequantise in registers (byte-permute lookups, exact bf16 products) and
-//            store the bf16 tile in the tensor-core operand layout; window rows are
-//            copied with cp.async;
-//   S^T      two threads issue 32 tcgen05.mma kind::f16 (M = 128 keys, N = 64 heads,
+// Design: two CTAs of 8 warps per query, each owning 32 of the 64 heads (heads are
+// independent, so the halves exchange nothing); 5 key tiles of 128 keys, the window
+// tile first:
+//   prefetch the 288-byte records of the next selected tile go to a raw staging buffer
+//            with cp.async while the current tile is processed; the window rows (bf16)
+//            are copied straight into the key tile at the start;
+//   build    all warps dequantise the staged records (byte-permute lookups, exact bf16
+//            products) into the bf16 key tile in the tensor-core operand layout;
+//   S^T      two threads issue 32 tcgen05.mma kind::f16 (M = 128 keys, N = 32 heads,
 //            K = 512) into four partial TMEM sums;
-//   softmax  thread = key, 32 heads per thread: warp max reductions, a per-head
+//   softmax  thread = key, 16 heads per thread: warp max reductions, a per-head
 //            reference max that only moves when a tile exceeds it by 2^8 (then the
 //            TMEM accumulator and the running sums are rescaled), exp2, bf16 P^T to
 //            shared memory;
-//   O^T      32 tcgen05.mma (4 M-tiles of 128 output channels, N = 64 heads, K = 128
+//   O^T      32 tcgen05.mma (4 M-tiles of 128 output channels, N = 32 heads, K = 128
 //            keys) reading the SAME bf16 tile as an MN-major operand (K == V);
 //   epilogue O = O^T / l per head -> bf16, lse = ln(sum exp).
 #include "csa2_kernels.cuh"
@@ -25,11 +28,13 @@
 namespace csa2 {
 
 constexpr int kAttnThreads = 256;
-constexpr int kHeads = 64;
-constexpr uint32_t kKtBytes = 128 * 512 * 2;   // bf16 key tile
-constexpr uint32_t kQsBytes = 64 * 512 * 2;    // bf16 queries
-constexpr uint32_t kPsBytes = 128 * 64 * 2;    // bf16 P^T
-constexpr uint32_t kOCols = 0, kSCols = 256;   // TMEM columns: O^T 4 x 64, S^T 4 partial sums x 64
+constexpr int kHeads = 64;                          // query heads
+constexpr int kHH = 32;                             // heads per CTA
+constexpr uint32_t kKtBytes = 128 * 512 * 2;        // bf16 key tile
+constexpr uint32_t kQsBytes = kHH * 512 * 2;        // bf16 queries of this CTA's heads
+constexpr uint32_t kPsBytes = 128 * kHH * 2;        // bf16 P^T
+constexpr uint32_t kRawBytes = 128 * kKvBytes;      // staged FP4 records of one tile
+constexpr uint32_t kOCols = 0, kSCols = 256;        // TMEM columns: O^T 4 x 32, S^T 4 partial sums x 32
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 
 // Offset of element (row, col) in a [rows][512] bf16 operand tile stored as 8x8 core
@@ -58,17 +63,21 @@ __device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
   return *reinterpret_cast<const __nv_bfloat162*>(&both);
 }
 
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_newest_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Kt = smem;
   uint8_t* Qs = Kt + kKtBytes;
   uint8_t* Ps = Qs + kQsBytes;
-  float* ref = reinterpret_cast<float*>(Ps + kPsBytes);  // [64] reference max (log2 units)
-  float* alpha = ref + kHeads;                            // [64]
-  float* tmax = alpha + kHeads;                           // [4][64]
-  float* lred = tmax + 4 * kHeads;                        // [4][64]
-  int64_t* recoff = reinterpret_cast<int64_t*>(lred + 4 * kHeads);     // [512] record byte offsets, -1 = none
+  uint8_t* Raw = Ps + kPsBytes;
+  float* ref = reinterpret_cast<float*>(Raw + kRawBytes);  // [32] reference max (log2 units)
+  float* alpha = ref + kHH;                                 // [32]
+  float* tmax = alpha + kHH;                                // [4][32]
+  float* lred = tmax + 4 * kHH;                             // [4][32]
+  int64_t* recoff = reinterpret_cast<int64_t*>(lred + 4 * kHH);        // [512] record byte offsets, -1 = none
   int32_t* tile_cnt = reinterpret_cast<int32_t*>(recoff + CSA2_TOPK);  // [4] valid entries per selected tile
   uint64_t* mma_bar = reinterpret_cast<uint64_t*>(tile_cnt + 4);  // [2] one per MMA issuer
   uint64_t* drain = mma_bar + 2;                                    // [2]
@@ -76,7 +85,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   int32_t* flags = reinterpret_cast<int32_t*>(tmem_slot + 1);  // [0] abort, [1] rescale
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t qi = blockIdx.x;
+  const int64_t qi = blockIdx.x >> 1;
+  const int h0 = (blockIdx.x & 1) * kHH;  // first head of this CTA
   const int32_t nv = __ldg(a.n_visible + qi);
   const int32_t wl = max(0, min(CSA2_WIN, __ldg(a.win_len + qi)));
 
@@ -89,18 +99,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     flags[1] = 0;
     fence_mbar_init();
   }
-  if (tid < kHeads) ref[tid] = -INFINITY;
+  if (tid < kHH) ref[tid] = -INFINITY;
   if (warp == 0) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  // queries -> shared memory (operand layout, K-major over the 512 channels)
+  // queries of this CTA's heads, then the window rows, -> shared memory (operand
+  // layout, K-major over the 512 channels); two cp.async groups
   {
-    const __nv_bfloat16* qg = a.q + qi * kHeads * CSA2_D;
-    for (int c = tid; c < kHeads * 64; c += kAttnThreads) {
+    const __nv_bfloat16* qg = a.q + (qi * kHeads + h0) * CSA2_D;
+    for (int c = tid; c < kHH * 64; c += kAttnThreads) {
       const uint32_t h = c >> 6, ch = c & 63;
       cp_async16(smem_u32(Qs + tile_off(h, ch * 8)), qg + h * CSA2_D + ch * 8, 16);
     }
+    cp_async_commit();
+    const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
+    for (int c = tid; c < 128 * 64; c += kAttnThreads) {
+      const uint32_t r = c >> 6, ch = c & 63;
+      const bool ok = static_cast<int32_t>(r) < wl;
+      cp_async16(smem_u32(Kt + tile_off(r, ch * 8)), ok ? static_cast<const void*>(wg + r * CSA2_D + ch * 8)
+                                                         : static_cast<const void*>(a.window),
+                 ok ? 16u : 0u);
+    }
+    cp_async_commit();
   }
   // offsets of the 512 selected records (one round trip for all indices)
   if (tid < 4) tile_cnt[tid] = 0;
@@ -125,48 +146,55 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
-  const uint32_t idesc_o = idesc_bf16(128, 64, 1, 1);
+  const uint32_t idesc_s = idesc_bf16(128, kHH, 0, 0);
+  const uint32_t idesc_o = idesc_bf16(128, kHH, 1, 1);
 
-  float lsum[32];
+  // Stages the records of selected tile t (16-byte pieces; a missing record reads as zeros).
+  auto prefetch = [&](int t) {
+    for (int c = tid; c < 128 * (kKvBytes / 16); c += kAttnThreads) {
+      const int slot = c / (kKvBytes / 16), j = c - slot * (kKvBytes / 16);
+      const int64_t off = recoff[t * 128 + slot];
+      cp_async16(smem_u32(Raw + slot * kKvBytes + j * 16), a.cache.kv + (off >= 0 ? off + j * 16 : 0),
+                 off >= 0 ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  auto next_selected = [&](int t) {  // first selected tile after t with any entry, or 4
+    int u = t + 1;
+    while (u < 4 && tile_cnt[u] == 0) ++u;
+    return u;
+  };
+  int staged = next_selected(-1);
+  if (staged < 4) prefetch(staged);
+
+  float lsum[16];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) lsum[i] = 0.0f;
+  for (int i = 0; i < 16; ++i) lsum[i] = 0.0f;
   uint32_t phase = 0;
   bool o_started = false;
-  const int hb = (warp >> 2) * 32;                 // this thread's 32 heads
-  const uint32_t key_row = (warp & 3) * 32 + lane; // TMEM lane = key (softmax) / channel (epilogue)
+  const int hb = (warp >> 2) * 16;                  // this thread's 16 heads (of the CTA's 32)
+  const uint32_t key_row = (warp & 3) * 32 + lane;  // TMEM lane = key (softmax) / channel (epilogue)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-  for (int t = 0; t < 5; ++t) {
-    // ---------------------------------------------------------------- build the key tile
+  for (int it = 0; it < 5; ++it) {
+    // ---------------------------------------------------------------- the key tile
+    const int t = it == 0 ? 4 : staged;  // the window first, then the selected tiles in order
+    if (t == 4 && it > 0) break;         // no selected tile left
     if (t == 4) {
-      const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
-      for (int c = tid; c < 128 * 64; c += kAttnThreads) {
-        const uint32_t r = c >> 6, ch = c & 63;
-        const bool ok = static_cast<int32_t>(r) < wl;
-        cp_async16(smem_u32(Kt + tile_off(r, ch * 8)), ok ? static_cast<const void*>(wg + r * CSA2_D + ch * 8)
-                                                           : static_cast<const void*>(a.window),
-                   ok ? 16u : 0u);
-      }
+      if (staged < 4) cp_async_wait_newest_pending();  // queries and window landed; records may still fly
+      else cp_async_wait_all();
     } else {
-      if (tile_cnt[t] == 0) continue;  // block-uniform: nothing selected in this tile
-      uint4 nib[8];
-      uint32_t scw[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int task = tid + kAttnThreads * i;
-        const int slot = task >> 4, j = task & 15;
-        const int64_t off = recoff[t * 128 + slot];
-        const uint8_t* rec = a.cache.kv + (off >= 0 ? off : 0);
-        nib[i] = off >= 0 ? __ldg(reinterpret_cast<const uint4*>(rec) + j) : make_uint4(0, 0, 0, 0);
-        scw[i] = off >= 0 ? __ldg(reinterpret_cast<const uint16_t*>(rec + 256) + j) : 0u;
-      }
+      cp_async_wait_all();
+      __syncthreads();  // every thread's pieces of the staged records are visible
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int task = tid + kAttnThreads * i;
         const uint32_t slot = task >> 4, j = task & 15;
-        const __nv_bfloat162 s0 = e4m3_bf16x2(scw[i] & 0xFFu), s1 = e4m3_bf16x2(scw[i] >> 8);
-        const uint32_t wds[4] = {nib[i].x, nib[i].y, nib[i].z, nib[i].w};
+        const uint8_t* rec = Raw + slot * kKvBytes;
+        const uint4 nib = *reinterpret_cast<const uint4*>(rec + j * 16);
+        const uint32_t scw = *reinterpret_cast<const uint16_t*>(rec + 256 + j * 2);
+        const __nv_bfloat162 s0 = e4m3_bf16x2(scw & 0xFFu), s1 = e4m3_bf16x2(scw >> 8);
+        const uint32_t wds[4] = {nib.x, nib.y, nib.z, nib.w};
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           uint32_t o[4];
@@ -175,11 +203,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         }
       }
     }
-    cp_async_wait_all();
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (t != 4) {  // the staging buffer is free again: fetch the next selected tile
+      staged = next_selected(t);
+      if (staged < 4) prefetch(staged);
+    }
 
     // ---------------------------------------------------------------- S^T = K Q^T
     // two issuing threads (warps 0 and 1): issuer i takes K-steps kk = i, i+2, ... into
@@ -189,7 +220,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       const uint32_t kb = smem_u32(Kt), qb = smem_u32(Qs);
 #pragma unroll 4
       for (uint32_t kk = me; kk < 32; kk += 2)
-        mma_bf16(tmem + kSCols + (kk & 3u) * 64u, sdesc(kb + kk * 256u, 128, 8192), sdesc(qb + kk * 256u, 128, 8192),
+        mma_bf16(tmem + kSCols + (kk & 3u) * kHH, sdesc(kb + kk * 256u, 128, 8192), sdesc(qb + kk * 256u, 128, 8192),
                  idesc_s, kk >= 4 ? 1u : 0u);
       mma_commit(&mma_bar[me]);
       if (!mbar_wait(&mma_bar[me], phase, nullptr)) {
@@ -204,32 +235,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
 
     // ---------------------------------------------------------------- softmax
     const bool kv_ok = t == 4 ? static_cast<int32_t>(key_row) < wl : recoff[t * 128 + key_row] >= 0;
-    float x[32];
+    float x[16];
     {
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_base + kSCols + static_cast<uint32_t>(hb), r);
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_base + kSCols + static_cast<uint32_t>(hb), r);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+      for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(r[i]);
 #pragma unroll
       for (uint32_t pp = 1; pp < 4; ++pp) {
-        tmem_ld32(tmem + lane_base + kSCols + pp * 64u + static_cast<uint32_t>(hb), r);
+        tmem_ld16(tmem + lane_base + kSCols + pp * kHH + static_cast<uint32_t>(hb), r);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] += __uint_as_float(r[i]);
+        for (int i = 0; i < 16; ++i) x[i] += __uint_as_float(r[i]);
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = kv_ok ? x[i] * a.scale_log2 : -INFINITY;
+      for (int i = 0; i < 16; ++i) x[i] = kv_ok ? x[i] * a.scale_log2 : -INFINITY;
     }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < 16; ++i) {
       const float m = redux_max(x[i]);
-      if (lane == i) tmax[(warp & 3) * kHeads + hb + i] = m;
+      if (lane == i) tmax[(warp & 3) * kHH + hb + i] = m;
     }
     if (tid == 0) flags[1] = 0;
     __syncthreads();
-    if (tid < kHeads) {
-      const float mt = fmaxf(fmaxf(tmax[tid], tmax[kHeads + tid]), fmaxf(tmax[2 * kHeads + tid], tmax[3 * kHeads + tid]));
+    if (tid < kHH) {
+      const float mt = fmaxf(fmaxf(tmax[tid], tmax[kHH + tid]), fmaxf(tmax[2 * kHH + tid], tmax[3 * kHH + tid]));
       const float old = ref[tid];
       float nw = old;
       if (mt > old + kRescaleThreshold || (old == -INFINITY && mt != -INFINITY)) nw = mt;
@@ -241,25 +272,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     if (flags[1] && o_started) {
       // rescale O^T columns (heads) and the running sums by alpha
 #pragma unroll
-      for (int i = 0; i < 32; ++i) lsum[i] *= alpha[hb + i];
+      for (int i = 0; i < 16; ++i) lsum[i] *= alpha[hb + i];
       for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
-        for (int h0 = 0; h0 < 64; h0 += 32) {
-          uint32_t r[32];
-          const uint32_t addr = tmem + lane_base + kOCols + static_cast<uint32_t>(c * 64 + h0);
-          tmem_ld32(addr, r);
-          tmem_ld_wait();
+        uint32_t r[32];
+        const uint32_t addr = tmem + lane_base + kOCols + static_cast<uint32_t>(c * kHH);
+        tmem_ld32(addr, r);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha[h0 + i]);
-          tmem_st32(addr, r);
-        }
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha[i]);
+        tmem_st32(addr, r);
       }
       tmem_st_wait();
     }
     // P = exp2(x - ref) -> bf16, P^T tile (MN-major: 8 heads x 2 bytes per core row)
     {
-      uint32_t pk[16];
+      uint32_t pk[8];
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
+      for (int i = 0; i < 16; i += 2) {
         const float r0 = ref[hb + i], r1 = ref[hb + i + 1];
         const float p0 = (r0 == -INFINITY) ? 0.0f : exp2f(x[i] - r0);
         const float p1 = (r1 == -INFINITY) ? 0.0f : exp2f(x[i + 1] - r1);
@@ -269,8 +298,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         pk[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t off = (key_row >> 3) * 1024u + static_cast<uint32_t>((hb >> 3) + c) * 128u + (key_row & 7u) * 16u;
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t off = (key_row >> 3) * (kHH * 16u) + static_cast<uint32_t>((hb >> 3) + c) * 128u +
+                             (key_row & 7u) * 16u;
         *reinterpret_cast<uint4*>(Ps + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
     }
@@ -287,8 +317,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       for (uint32_t kk = 0; kk < 8; ++kk) {
 #pragma unroll
         for (uint32_t c = 2 * me; c < 2 * me + 2; ++c)
-          mma_bf16(tmem + kOCols + c * 64u, sdesc(kb + c * 2048u + kk * 16384u, 8192, 128),
-                   sdesc(pb + kk * 2048u, 1024, 128), idesc_o, (o_started || kk > 0) ? 1u : 0u);
+          mma_bf16(tmem + kOCols + c * kHH, sdesc(kb + c * 2048u + kk * 16384u, 8192, 128),
+                   sdesc(pb + kk * (2u * kHH * 16u), kHH * 16u, 128), idesc_o, (o_started || kk > 0) ? 1u : 0u);
       }
       mma_commit(&mma_bar[me]);
       if (!mbar_wait(&mma_bar[me], phase, nullptr)) {
@@ -302,48 +332,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     tc_fence_after();
     if (flags[0]) break;
   }
+  cp_async_wait_all();  // no copy may land after the CTA is gone
 
   // ---------------------------------------------------------------- epilogue
   if (!flags[0]) {
     // row sums: reduce the 128 key slots of each head
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < 16; ++i) {
       float v = lsum[i];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == i) lred[(warp & 3) * kHeads + hb + i] = v;
+      if (lane == i) lred[(warp & 3) * kHH + hb + i] = v;
     }
     __syncthreads();
-    if (tid < kHeads) {
-      const float l = lred[tid] + lred[kHeads + tid] + lred[2 * kHeads + tid] + lred[3 * kHeads + tid];
-      alpha[tid] = l;  // reuse: final row sum
-      if (a.lse) a.lse[qi * kHeads + tid] = (l > 0.0f) ? (ref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    if (tid < kHH) {
+      const float l = lred[tid] + lred[kHH + tid] + lred[2 * kHH + tid] + lred[3 * kHH + tid];
+      if (a.lse)
+        a.lse[qi * kHeads + h0 + tid] = (l > 0.0f) ? (ref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      alpha[tid] = l > 0.0f ? 1.0f / l : 0.0f;  // reuse: 1 / row sum
     }
     __syncthreads();
-    // O^T (TMEM lane = channel, column = head) -> bf16 [64][512] staged in the free key
+    // O^T (TMEM lane = channel, column = head) -> bf16 [32][512] staged in the free key
     // tile, then written out with 16-byte coalesced stores
     __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(Kt);
-    if (tid < kHeads) alpha[tid] = alpha[tid] > 0.0f ? 1.0f / alpha[tid] : 0.0f;  // 1 / row sum
-    __syncthreads();
     for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
       const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
-      for (int h0 = 0; h0 < 64; h0 += 32) {
-        uint32_t r[32];
-        if (o_started) {
-          tmem_ld32(tmem + lane_base + kOCols + static_cast<uint32_t>(c * 64 + h0), r);
-          tmem_ld_wait();
-        }
+      uint32_t r[32];
+      if (o_started) {
+        tmem_ld32(tmem + lane_base + kOCols + static_cast<uint32_t>(c * kHH), r);
+        tmem_ld_wait();
+      }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float o = o_started ? __uint_as_float(r[i]) * alpha[h0 + i] : 0.0f;
-          ostage[(h0 + i) * CSA2_D + d] = __float2bfloat16_rn(o);
-        }
+      for (int i = 0; i < 32; ++i) {
+        const float o = o_started ? __uint_as_float(r[i]) * alpha[i] : 0.0f;
+        ostage[i * CSA2_D + d] = __float2bfloat16_rn(o);
       }
     }
     __syncthreads();
-    uint4* og = reinterpret_cast<uint4*>(a.out + qi * kHeads * CSA2_D);
+    uint4* og = reinterpret_cast<uint4*>(a.out + (qi * kHeads + h0) * CSA2_D);
     const uint4* os = reinterpret_cast<const uint4*>(ostage);
-    for (int i = tid; i < kHeads * CSA2_D / 8; i += kAttnThreads) og[i] = os[i];
+    for (int i = tid; i < kHH * CSA2_D / 8; i += kAttnThreads) og[i] = os[i];
   }
   // drain outstanding MMAs, then free TMEM
   if (lane == 0 && warp < 2) {
@@ -357,7 +385,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
 }
 
 size_t attn_smem_bytes() {
-  return 1024 + kKtBytes + kQsBytes + kPsBytes + (2 + 8) * kHeads * sizeof(float) + 80 + CSA2_TOPK * 8 + 16;
+  return 1024 + kKtBytes + kQsBytes + kPsBytes + kRawBytes + (2 + 8) * kHH * sizeof(float) + CSA2_TOPK * 8 + 16 +
+         4 * sizeof(uint64_t) + 16;
 }
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
@@ -366,7 +395,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
   static std::atomic<int> limit_set[kMaxDevices];
   cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(attn_kernel), smem, limit_set);
   if (e != cudaSuccess) return e;
-  attn_kernel<<<static_cast<unsigned>(a.n_q), kAttnThreads, smem, stream>>>(a);
+  attn_kernel<<<static_cast<unsigned>(2 * a.n_q), kAttnThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
