@@ -43,6 +43,16 @@ __device__ __forceinline__ uint32_t tile_off(uint32_t row, uint32_t col) {
   return (row >> 3) * 8192u + (col >> 3) * 128u + (row & 7u) * 16u + (col & 7u) * 2u;
 }
 
+// Work item c of a [rows][64 chunks of 16 bytes] tile -> (row, chunk).  A warp's 32
+// items cover 8 consecutive rows x 4 consecutive chunks: each group of 8 lanes writes
+// one 128-byte line of the core-matrix layout (no bank conflicts), and each row's 4
+// chunks are 64 contiguous bytes of the source row (whole 32-byte sectors).
+__device__ __forceinline__ void tile_item(uint32_t c, uint32_t rows, uint32_t& row, uint32_t& chunk) {
+  const uint32_t rg = rows >> 3;  // row groups
+  row = (c & 7u) | (((c >> 5) % rg) << 3);
+  chunk = ((c >> 3) & 3u) | ((c >> 5) / rg << 2);
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t sdst, const void* gsrc, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sdst), "l"(gsrc), "r"(src_bytes) : "memory");
 }
@@ -109,13 +119,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   {
     const __nv_bfloat16* qg = a.q + (qi * kHeads + h0) * CSA2_D;
     for (int c = tid; c < kHH * 64; c += kAttnThreads) {
-      const uint32_t h = c >> 6, ch = c & 63;
+      uint32_t h, ch;
+      tile_item(static_cast<uint32_t>(c), kHH, h, ch);
       cp_async16(smem_u32(Qs + tile_off(h, ch * 8)), qg + h * CSA2_D + ch * 8, 16);
     }
     cp_async_commit();
     const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
     for (int c = tid; c < 128 * 64; c += kAttnThreads) {
-      const uint32_t r = c >> 6, ch = c & 63;
+      uint32_t r, ch;
+      tile_item(static_cast<uint32_t>(c), 128, r, ch);
       const bool ok = static_cast<int32_t>(r) < wl;
       cp_async16(smem_u32(Kt + tile_off(r, ch * 8)), ok ? static_cast<const void*>(wg + r * CSA2_D + ch * 8)
                                                          : static_cast<const void*>(a.window),
@@ -186,10 +198,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     } else {
       cp_async_wait_all();
       __syncthreads();  // every thread's pieces of the staged records are visible
+      // item = (entry slot, 32-channel block j); a warp takes 8 slots x 4 blocks so that
+      // its 16-byte tile stores fill whole 128-byte lines
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int task = tid + kAttnThreads * i;
-        const uint32_t slot = task >> 4, j = task & 15;
+        const uint32_t task = static_cast<uint32_t>(tid + kAttnThreads * i);
+        const uint32_t slot = (task & 7u) | (((task >> 5) & 15u) << 3);
+        const uint32_t j = ((task >> 3) & 3u) | ((task >> 9) << 2);
         const uint8_t* rec = Raw + slot * kKvBytes;
         const uint4 nib = *reinterpret_cast<const uint4*>(rec + j * 16);
         const uint32_t scw = *reinterpret_cast<const uint16_t*>(rec + 256 + j * 2);
