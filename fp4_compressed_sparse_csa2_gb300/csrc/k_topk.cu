@@ -409,7 +409,8 @@ cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes) {
 // polling: the only waits are hardware cluster barriers.
 namespace csa2 {
 
-constexpr int kClCandCap = 8192;
+constexpr int kClCandCap = 4096;   // leader: candidates of the threshold bin
+constexpr int kClLocalCap = 1024;  // per CTA: staged candidates of the threshold bin
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -453,16 +454,52 @@ __device__ __forceinline__ uint32_t dsmem_append(uint32_t counter, bool pred) {
   return base + __popc(m & ((1u << lane) - 1u));
 }
 
+// Sorts the k = 512 distinct indices in v (one per thread; padding INT_MAX) ascending
+// and writes the first k to out: each warp sorts its 32 with a shuffle network, then an
+// element's position is the number of smaller elements over all 16 sorted runs (binary
+// searches), so only one block barrier is needed.
+__device__ void sort_indices_out(int32_t v, int32_t* runs, int32_t* out, int k) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool up = (lane & size) == 0 || size == 32;
+      const bool low = (lane & stride) == 0;
+      v = (low == up) ? min(v, o) : max(v, o);
+    }
+  }
+  runs[threadIdx.x] = v;
+  __syncthreads();
+  int pos = lane;  // smaller elements of this warp's run
+  for (int w = 0; w < kTopkThreads / 32; ++w) {
+    if (w == warp) continue;
+    const int32_t* r = runs + 32 * w;
+    int lo = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)
+      if (r[lo + step - 1] < v) lo += step;
+    if (r[lo] < v) ++lo;
+    pos += lo;
+  }
+  if (pos < k && v != INT_MAX) out[pos] = v;
+}
+
 __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkArgs a, int64_t chunk) {
   extern __shared__ __align__(16) uint8_t tc_smem[];
-  uint32_t* h = reinterpret_cast<uint32_t*>(tc_smem);   // [kBins] this CTA's histogram
-  uint32_t* hsum = h + kBins;                           // [kBins] row histogram
-  uint32_t* ctr = hsum + kBins;                         // [4] leader: selected, candidates, picked
-  int32_t* sel = reinterpret_cast<int32_t*>(ctr + 4);   // [512] leader: chosen indices
-  uint2* cand = reinterpret_cast<uint2*>(sel + 512);    // [kClCandCap] leader: (key, index)
+  uint32_t* h = reinterpret_cast<uint32_t*>(tc_smem);  // [2][kBins] this CTA's histograms (lane parity)
+  uint32_t* hsum = h + 2 * kBins;                      // [kBins] row histogram
+  uint32_t* ctr = hsum + kBins;                        // [4] leader: selected, candidates, picked, overflow
+  uint32_t* lctr = ctr + 4;                            // [4] this CTA: staged selected, staged candidates
+  int32_t* sel = reinterpret_cast<int32_t*>(lctr + 4);  // [512] leader: chosen indices
+  int32_t* lsel = sel + 512;                            // [512] this CTA: indices above the threshold bin
+  uint2* cand = reinterpret_cast<uint2*>(lsel + 512);   // [kClCandCap] leader: (key, index)
+  uint2* lcand = cand + kClCandCap;                     // [kClLocalCap] this CTA: (key, index)
   __shared__ uint32_t s_warp[32];
   __shared__ int s_bin;
   __shared__ uint32_t s_above;
+  __shared__ uint32_t s_base[2];
   const uint32_t rank = cluster_rank();
   const uint32_t csize = gridDim.x;  // one cluster spans the x dimension
   const int64_t q = blockIdx.y;
@@ -475,10 +512,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
   }
   const int64_t c0 = static_cast<int64_t>(rank) * chunk;
   const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
-  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
-  if (threadIdx.x < 4) ctr[threadIdx.x] = 0;
+  for (int b = threadIdx.x; b < 2 * kBins; b += kTopkThreads) h[b] = 0;
+  if (threadIdx.x < 8) ctr[threadIdx.x] = 0;  // ctr and lctr
   __syncthreads();
   const float* row = a.scores + q * a.ld;
+  uint32_t* hl = h + (threadIdx.x & 1) * kBins;  // two copies halve the atomic contention on busy bins
   // ---- pass 1: histogram of the top 11 key bits (4 float4 per thread in flight)
   for (int64_t base = c0; base < c1; base += 16 * kTopkThreads) {
     float4 v[4];
@@ -497,12 +535,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
-      if (i0 + 0 < c1) atomicAdd(&h[order_key(v[u].x) >> 21], 1u);
-      if (i0 + 1 < c1) atomicAdd(&h[order_key(v[u].y) >> 21], 1u);
-      if (i0 + 2 < c1) atomicAdd(&h[order_key(v[u].z) >> 21], 1u);
-      if (i0 + 3 < c1) atomicAdd(&h[order_key(v[u].w) >> 21], 1u);
+      if (i0 + 0 < c1) atomicAdd(&hl[order_key(v[u].x) >> 21], 1u);
+      if (i0 + 1 < c1) atomicAdd(&hl[order_key(v[u].y) >> 21], 1u);
+      if (i0 + 2 < c1) atomicAdd(&hl[order_key(v[u].z) >> 21], 1u);
+      if (i0 + 3 < c1) atomicAdd(&hl[order_key(v[u].w) >> 21], 1u);
     }
   }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] += h[kBins + b];
   cluster_sync_all();  // every CTA's histogram and the leader's counters are ready
   for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
     uint32_t sum = 0;
@@ -512,8 +552,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
   __syncthreads();
   threshold_bin(hsum, static_cast<uint32_t>(a.k), &s_bin, &s_above, s_warp);
   const uint32_t bstar = static_cast<uint32_t>(s_bin);
-  // ---- pass 2: append to the leader (the chunk is mostly still in L2)
-  const uint32_t l_ctr = dsmem_map(&ctr[0], 0), l_sel = dsmem_map(sel, 0), l_cand = dsmem_map(cand, 0);
+  // ---- pass 2: stage this chunk's entries above / in the threshold bin locally (the
+  // chunk is mostly still in L2), then hand them to the leader in one block copy
   for (int64_t base = c0; base < c1; base += 16 * kTopkThreads) {
     float4 v[4];
 #pragma unroll
@@ -541,15 +581,31 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
         const bool in = i0 + j < c1;
         const uint32_t bin = key[j] >> 21;
         const bool hi = in && bin > bstar;
-        uint32_t slot = dsmem_append(l_ctr, hi);
-        if (hi && slot < static_cast<uint32_t>(a.k)) dsmem_st(l_sel + 4u * slot, static_cast<uint32_t>(i0 + j));
+        uint32_t slot = 0;
+        append(&lctr[0], hi, slot);
+        if (hi && slot < static_cast<uint32_t>(a.k)) lsel[slot] = static_cast<int32_t>(i0 + j);
         const bool eq = in && bin == bstar;
-        slot = dsmem_append(l_ctr + 4u, eq);
-        if (eq && slot < kClCandCap) dsmem_st2(l_cand + 8u * slot, key[j], static_cast<uint32_t>(i0 + j));
+        append(&lctr[1], eq, slot);
+        if (eq && slot < kClLocalCap) lcand[slot] = make_uint2(key[j], static_cast<uint32_t>(i0 + j));
       }
     }
   }
-  cluster_sync_all();  // every append has landed in the leader
+  __syncthreads();
+  const uint32_t l_ctr = dsmem_map(&ctr[0], 0), l_sel = dsmem_map(sel, 0), l_cand = dsmem_map(cand, 0);
+  const uint32_t n_hi = lctr[0] < static_cast<uint32_t>(a.k) ? lctr[0] : static_cast<uint32_t>(a.k);
+  const uint32_t n_eq = lctr[1];
+  if (threadIdx.x == 0) {
+    s_base[0] = n_hi ? dsmem_atom_add(l_ctr, n_hi) : 0u;
+    s_base[1] = n_eq ? dsmem_atom_add(l_ctr + 4u, n_eq) : 0u;
+    if (n_eq > kClLocalCap) dsmem_st(l_ctr + 12u, 1u);  // a staged list overflowed: the leader refines the row
+  }
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < n_hi; i += kTopkThreads)
+    if (s_base[0] + i < static_cast<uint32_t>(a.k)) dsmem_st(l_sel + 4u * (s_base[0] + i), static_cast<uint32_t>(lsel[i]));
+  const uint32_t n_eq_st = n_eq < kClLocalCap ? n_eq : kClLocalCap;
+  for (uint32_t i = threadIdx.x; i < n_eq_st; i += kTopkThreads)
+    if (s_base[1] + i < kClCandCap) dsmem_st2(l_cand + 8u * (s_base[1] + i), lcand[i].x, lcand[i].y);
+  cluster_sync_all();  // every hand-off has landed in the leader
   if (rank != 0) return;
   // ---- leader: resolve the threshold bin exactly
   const uint32_t above = s_above, nc = hsum[bstar], need = static_cast<uint32_t>(a.k) - above;
@@ -560,7 +616,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
   __syncthreads();
   uint32_t* hA = h;  // reuse this CTA's histogram as scratch
   bool done = false;
-  if (nc <= kClCandCap) {
+  if (nc <= kClCandCap && ctr[3] == 0) {
     // level A: bits [10, 21) below the 11-bit prefix
     for (int b = threadIdx.x; b < kBins; b += kTopkThreads) hA[b] = 0;
     __syncthreads();
@@ -597,7 +653,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
       while (p2 < static_cast<int>(n_ties)) p2 <<= 1;
       for (int i = static_cast<int>(n_ties) + threadIdx.x; i < p2; i += kTopkThreads) ties[i] = 0x7FFFFFFF;
       __syncthreads();
-      bitonic_sort(ties, p2);
+      if (n_ties > 1) bitonic_sort(ties, p2);
       const uint32_t base = above + (need - needB);
       for (uint32_t i = threadIdx.x; i < needB; i += kTopkThreads) sel[base + i] = ties[i];
       __syncthreads();
@@ -605,45 +661,67 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
     }
   }
   if (!done) {
-    // massive ties: exact radix refinement over the whole row
+    // massive ties or an overflowing hand-off: exact radix refinement over the whole row
+    if (threadIdx.x == 0) ctr[2] = above;
+    __syncthreads();
     refine_row(a, q, nv, bstar, need, h, s_warp, sel, &ctr[2]);
     __syncthreads();
   }
-  bitonic_sort(sel, a.k);
-  for (int i = threadIdx.x; i < a.k; i += kTopkThreads) out[i] = sel[i];
+  sort_indices_out(threadIdx.x < a.k ? sel[threadIdx.x] : INT_MAX, reinterpret_cast<int32_t*>(hsum), out, a.k);
 }
 
 size_t topk_cluster_smem() {
-  return 2 * kBins * sizeof(uint32_t) + 4 * sizeof(uint32_t) + 512 * sizeof(int32_t) + kClCandCap * sizeof(uint2);
+  return 3 * kBins * sizeof(uint32_t) + 8 * sizeof(uint32_t) + 2 * 512 * sizeof(int32_t) +
+         (kClCandCap + kClLocalCap) * sizeof(uint2);
 }
 
 cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream) {
   if (a.n_q == 0) return cudaSuccess;
-  // cluster size: enough CTAs to fill the GPU about twice, at most 8 (portable), and
-  // chunks of at least 8K entries
-  int64_t c = (2 * static_cast<int64_t>(sm_count) + a.n_q - 1) / a.n_q;
-  const int64_t by_len = (a.t_max + 8191) / 8192;
-  if (c > by_len) c = by_len;
-  if (c < 1) c = 1;
-  if (c > 8) c = 8;
-  int64_t chunk = (a.t_max + c - 1) / c;
-  chunk = ((chunk + 2047) / 2048) * 2048;
   const size_t smem = topk_cluster_smem();
   static std::atomic<int> limit_set[kMaxDevices];
   cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(topk_cluster_kernel), smem, limit_set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(c), static_cast<unsigned>(a.n_q), 1);
   cfg.blockDim = dim3(kTopkThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(c);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // Cluster size: the largest of 8, 4, 2, 1 whose clusters for all rows are resident at
+  // once (one wave), with chunks of at least 8K entries; the resident-cluster counts are
+  // queried once per device.
+  static std::atomic<int> active[kMaxDevices][4];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int64_t by_len = (a.t_max + 8191) / 8192;
+  int64_t c = 1;
+  for (int lg = 3; lg >= 0; --lg) {
+    const int64_t cc = int64_t(1) << lg;
+    if (cc > by_len && cc > 1) continue;
+    int n_act = (dev >= 0 && dev < kMaxDevices) ? active[dev][lg].load(std::memory_order_relaxed) : 0;
+    if (n_act == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(cc), 1, 1);
+      attr[0].val.clusterDim.x = static_cast<unsigned>(cc);
+      if (cudaOccupancyMaxActiveClusters(&n_act, topk_cluster_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n_act = -1;
+      }
+      if (dev >= 0 && dev < kMaxDevices) active[dev][lg].store(n_act == 0 ? -1 : n_act, std::memory_order_relaxed);
+    }
+    if (n_act > 0 && n_act >= a.n_q) {
+      c = cc;
+      break;
+    }
+  }
+  (void)sm_count;
+  int64_t chunk = (a.t_max + c - 1) / c;
+  chunk = ((chunk + 2047) / 2048) * 2048;
+  cfg.gridDim = dim3(static_cast<unsigned>(c), static_cast<unsigned>(a.n_q), 1);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(c);
   return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a, chunk);
 }
 
