@@ -411,6 +411,7 @@ namespace csa2 {
 
 constexpr int kClCandCap = 4096;   // leader: candidates of the threshold bin
 constexpr int kClLocalCap = 1024;  // per CTA: staged candidates of the threshold bin
+constexpr int kClBlockCap = 4096;  // per CTA: block maxima (32-entry blocks) of the chunk
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -473,35 +474,145 @@ __device__ void sort_indices_out(int32_t v, int32_t* runs, int32_t* out, int k) 
   runs[threadIdx.x] = v;
   __syncthreads();
   int pos = lane;  // smaller elements of this warp's run
-  for (int w = 0; w < kTopkThreads / 32; ++w) {
-    if (w == warp) continue;
-    const int32_t* r = runs + 32 * w;
-    int lo = 0;
+  int lo[kTopkThreads / 32];  // the 15 searches are independent: run them side by side
 #pragma unroll
-    for (int step = 16; step > 0; step >>= 1)
-      if (r[lo + step - 1] < v) lo += step;
-    if (r[lo] < v) ++lo;
-    pos += lo;
+  for (int w = 0; w < kTopkThreads / 32; ++w) lo[w] = 0;
+#pragma unroll
+  for (int step = 16; step > 0; step >>= 1) {
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w)
+      if (runs[32 * w + lo[w] + step - 1] < v) lo[w] += step;
   }
+#pragma unroll
+  for (int w = 0; w < kTopkThreads / 32; ++w)
+    if (w != warp) pos += lo[w] + (runs[32 * w + lo[w]] < v ? 1 : 0);
   if (pos < k && v != INT_MAX) out[pos] = v;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkArgs a, int64_t chunk) {
+// Exact selection among candidate (key, index) pairs that contain the `need` largest
+// keys: three radix levels (11 + 11 + 10 bits) give the key v* of the need-th largest;
+// keys above v* are taken, then the lowest indices among keys equal to v*.  Appends to
+// sel starting at *n_picked.  h: kBins scratch; ties: kBins scratch.  Returns false
+// (nothing written) when the ties at v* do not fit.
+__device__ bool select_candidates(const uint2* cand, uint32_t nc, uint32_t need, uint32_t* h, int32_t* ties,
+                                  uint32_t* s_warp, int32_t* sel, uint32_t* n_picked, uint32_t* n_ties_ctr) {
+  __shared__ int s_bin;
+  __shared__ uint32_t s_above;
+  uint32_t prefix = 0, need_l = need;
+  int pbits = 0;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+#pragma unroll 1
+  for (int lv = 0; lv < 3; ++lv) {
+    const int sh = shifts[lv], wd = widths[lv];
+    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
+      const uint32_t key = cand[i].x;
+      if (pbits == 0 || (key >> (32 - pbits)) == prefix) atomicAdd(&h[(key >> sh) & ((1u << wd) - 1u)], 1u);
+    }
+    __syncthreads();
+    threshold_bin(h, need_l, &s_bin, &s_above, s_warp);
+    need_l -= s_above;
+    prefix = (prefix << wd) | static_cast<uint32_t>(s_bin);
+    pbits += wd;
+  }
+  const uint32_t vstar = prefix, n_ties = h[s_bin];
+  __syncthreads();
+  if (n_ties > static_cast<uint32_t>(kBins)) return false;  // block-uniform
+  const uint32_t start = *n_picked;
+  if (threadIdx.x == 0) *n_ties_ctr = 0;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
+    const uint2 c = cand[i];
+    if (c.x > vstar) sel[atomicAdd(n_picked, 1u)] = static_cast<int32_t>(c.y);
+    else if (c.x == vstar) ties[atomicAdd(n_ties_ctr, 1u)] = static_cast<int32_t>(c.y);
+  }
+  __syncthreads();
+  if (n_ties > 1) {
+    int p2 = 1;
+    while (p2 < static_cast<int>(n_ties)) p2 <<= 1;
+    for (int i = static_cast<int>(n_ties) + threadIdx.x; i < p2; i += kTopkThreads) ties[i] = 0x7FFFFFFF;
+    __syncthreads();
+    bitonic_sort(ties, p2);
+  }
+  const uint32_t base = start + (need - need_l);
+  for (uint32_t i = threadIdx.x; i < need_l; i += kTopkThreads) sel[base + i] = ties[i];
+  __syncthreads();
+  if (threadIdx.x == 0) *n_picked = start + need;
+  __syncthreads();
+  return true;
+}
+
+// Exact top-k of a whole row by one CTA (inputs whose candidates overflow the buffers):
+// the row's 11-bit histogram, the entries of higher bins, then refine_row.
+__device__ void full_row_select(const TopkArgs& a, int64_t q, int64_t nv, uint32_t* h, uint32_t* s_warp, int32_t* sel,
+                                uint32_t* n_picked) {
+  __shared__ int s_bin;
+  __shared__ uint32_t s_above;
+  const float* row = a.scores + q * a.ld;
+  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
+  __syncthreads();
+  for (int64_t i = threadIdx.x; i < nv; i += kTopkThreads) atomicAdd(&h[order_key(__ldg(row + i)) >> 21], 1u);
+  __syncthreads();
+  threshold_bin(h, static_cast<uint32_t>(a.k), &s_bin, &s_above, s_warp);
+  const uint32_t bstar = static_cast<uint32_t>(s_bin), above = s_above;
+  if (threadIdx.x == 0) *n_picked = 0;
+  __syncthreads();
+  for (int64_t base = 0; base < nv; base += kTopkThreads) {
+    const int64_t i = base + threadIdx.x;
+    const bool take = i < nv && (order_key(__ldg(row + i)) >> 21) > bstar;
+    uint32_t slot = 0;
+    append(n_picked, take, slot);
+    if (take && slot < static_cast<uint32_t>(a.k)) sel[slot] = static_cast<int32_t>(i);
+  }
+  __syncthreads();
+  refine_row(a, q, nv, bstar, static_cast<uint32_t>(a.k) - above, h, s_warp, sel, n_picked);
+  __syncthreads();
+}
+
+// Adds the lanes' entries flagged in msk (bit 4u + j = entry j of float4 u) to a
+// shared list with one packed warp scan and one shared atomic per warp.
+template <typename Emit>
+__device__ __forceinline__ void warp_append(uint32_t msk, uint32_t* counter, Emit emit) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t mine = static_cast<uint32_t>(__popc(msk));
+  uint32_t incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= static_cast<uint32_t>(off)) incl += o;
+  }
+  uint32_t b = 0;
+  if (lane == 31 && incl) b = atomicAdd(counter, incl);
+  b = __shfl_sync(0xffffffffu, b, 31);
+  uint32_t slot = b + incl - mine;
+  while (msk) {
+    const uint32_t bit = __ffs(msk) - 1;
+    emit(bit, slot);
+    ++slot;
+    msk &= msk - 1u;
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const TopkArgs a, int64_t chunk) {
   extern __shared__ __align__(16) uint8_t tc_smem[];
-  uint32_t* h = reinterpret_cast<uint32_t*>(tc_smem);  // [2][kBins] this CTA's histograms (lane parity)
+  uint32_t* h = reinterpret_cast<uint32_t*>(tc_smem);  // [2][kBins] histograms (lane parity); [1] later: block list
   uint32_t* hsum = h + 2 * kBins;                      // [kBins] row histogram
   uint32_t* ctr = hsum + kBins;                        // [4] leader: selected, candidates, picked, overflow
-  uint32_t* lctr = ctr + 4;                            // [4] this CTA: staged selected, staged candidates
+  uint32_t* lctr = ctr + 4;                            // [4] this CTA: staged selected, candidates, blocks, ties
   int32_t* sel = reinterpret_cast<int32_t*>(lctr + 4);  // [512] leader: chosen indices
   int32_t* lsel = sel + 512;                            // [512] this CTA: indices above the threshold bin
   uint2* cand = reinterpret_cast<uint2*>(lsel + 512);   // [kClCandCap] leader: (key, index)
   uint2* lcand = cand + kClCandCap;                     // [kClLocalCap] this CTA: (key, index)
+  uint32_t* bm = reinterpret_cast<uint32_t*>(lcand + kClLocalCap);  // [kClBlockCap] block maxima of the chunk
   __shared__ uint32_t s_warp[32];
   __shared__ int s_bin;
   __shared__ uint32_t s_above;
   __shared__ uint32_t s_base[2];
   const uint32_t rank = cluster_rank();
   const uint32_t csize = gridDim.x;  // one cluster spans the x dimension
+  const uint32_t lane = threadIdx.x & 31;
   const int64_t q = blockIdx.y;
   const int64_t nv = row_visible(a, q);
   int32_t* out = a.out + q * a.k;
@@ -512,12 +623,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
   }
   const int64_t c0 = static_cast<int64_t>(rank) * chunk;
   const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
+  // Long rows go by 32-entry block maxima: the k-th largest block maximum bounds the
+  // k-th largest key from below (k blocks each hold a key at least that large), so only
+  // blocks reaching the bound are read again.  Short rows histogram every key.
+  const bool by_blocks = (nv + 31) / 32 >= a.k && chunk / 32 <= kClBlockCap;  // uniform across the cluster
   for (int b = threadIdx.x; b < 2 * kBins; b += kTopkThreads) h[b] = 0;
   if (threadIdx.x < 8) ctr[threadIdx.x] = 0;  // ctr and lctr
   __syncthreads();
   const float* row = a.scores + q * a.ld;
   uint32_t* hl = h + (threadIdx.x & 1) * kBins;  // two copies halve the atomic contention on busy bins
-  // ---- pass 1: histogram of the top 11 key bits (4 float4 per thread in flight)
+  // ---- pass 1: histogram of the top 11 key bits of every key, or of every block maximum
   for (int64_t base = c0; base < c1; base += 16 * kTopkThreads) {
     float4 v[4];
 #pragma unroll
@@ -535,10 +650,26 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
-      if (i0 + 0 < c1) atomicAdd(&hl[order_key(v[u].x) >> 21], 1u);
-      if (i0 + 1 < c1) atomicAdd(&hl[order_key(v[u].y) >> 21], 1u);
-      if (i0 + 2 < c1) atomicAdd(&hl[order_key(v[u].z) >> 21], 1u);
-      if (i0 + 3 < c1) atomicAdd(&hl[order_key(v[u].w) >> 21], 1u);
+      if (by_blocks) {
+        // lanes 8g .. 8g + 7 hold the 32 entries of one block
+        uint32_t m = 0;
+        m = max(m, i0 + 0 < c1 ? order_key(v[u].x) : 0u);
+        m = max(m, i0 + 1 < c1 ? order_key(v[u].y) : 0u);
+        m = max(m, i0 + 2 < c1 ? order_key(v[u].z) : 0u);
+        m = max(m, i0 + 3 < c1 ? order_key(v[u].w) : 0u);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        if ((lane & 7u) == 0 && i0 < c1) {
+          bm[(i0 - c0) >> 5] = m;
+          atomicAdd(&hl[m >> 21], 1u);
+        }
+      } else {
+        if (i0 + 0 < c1) atomicAdd(&hl[order_key(v[u].x) >> 21], 1u);
+        if (i0 + 1 < c1) atomicAdd(&hl[order_key(v[u].y) >> 21], 1u);
+        if (i0 + 2 < c1) atomicAdd(&hl[order_key(v[u].z) >> 21], 1u);
+        if (i0 + 3 < c1) atomicAdd(&hl[order_key(v[u].w) >> 21], 1u);
+      }
     }
   }
   __syncthreads();
@@ -552,52 +683,103 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
   __syncthreads();
   threshold_bin(hsum, static_cast<uint32_t>(a.k), &s_bin, &s_above, s_warp);
   const uint32_t bstar = static_cast<uint32_t>(s_bin);
-  // ---- pass 2: stage this chunk's entries above / in the threshold bin locally (the
-  // chunk is mostly still in L2), then hand them to the leader in one block copy
-  for (int64_t base = c0; base < c1; base += 16 * kTopkThreads) {
-    float4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
-      if (i0 + 3 < c1) {
-        v[u] = __ldg(reinterpret_cast<const float4*>(row + i0));
-      } else {
-        v[u].x = i0 + 0 < c1 ? __ldg(row + i0 + 0) : 0.0f;
-        v[u].y = i0 + 1 < c1 ? __ldg(row + i0 + 1) : 0.0f;
-        v[u].z = i0 + 2 < c1 ? __ldg(row + i0 + 2) : 0.0f;
-        v[u].w = i0 + 3 < c1 ? __ldg(row + i0 + 3) : 0.0f;
-      }
+  if (by_blocks) {
+    // ---- pass 2 (blocks): list the chunk's blocks whose maximum reaches bin b*, then
+    // stage their keys of bin >= b* (8 lanes per block, 4 blocks per warp in flight)
+    uint32_t* blist = h + kBins;  // the second histogram copy is free now
+    // CTAs whose chunk starts past the row's end (c1 < c0) have no blocks
+    const uint32_t nb = c1 > c0 ? static_cast<uint32_t>((c1 - c0 + 31) >> 5) : 0u;
+    for (uint32_t base = 0; base < nb; base += kTopkThreads) {
+      const uint32_t i = base + threadIdx.x;
+      const bool take = i < nb && (bm[i] >> 21) >= bstar;
+      uint32_t slot = 0;
+      append(&lctr[2], take, slot);
+      if (take && slot < kBins) blist[slot] = i;
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
-      const uint32_t key[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w)};
-      bool any = false;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) any |= (i0 + j < c1) && (key[j] >> 21) >= bstar;
-      if (!__any_sync(0xffffffffu, any)) continue;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool in = i0 + j < c1;
-        const uint32_t bin = key[j] >> 21;
-        const bool hi = in && bin > bstar;
-        uint32_t slot = 0;
-        append(&lctr[0], hi, slot);
-        if (hi && slot < static_cast<uint32_t>(a.k)) lsel[slot] = static_cast<int32_t>(i0 + j);
-        const bool eq = in && bin == bstar;
-        append(&lctr[1], eq, slot);
-        if (eq && slot < kClLocalCap) lcand[slot] = make_uint2(key[j], static_cast<uint32_t>(i0 + j));
+    __syncthreads();
+    const uint32_t nbl = lctr[2] < static_cast<uint32_t>(kBins) ? lctr[2] : static_cast<uint32_t>(kBins);
+    const uint32_t warp = threadIdx.x >> 5, grp = lane >> 3;
+    for (uint32_t r0 = warp * 4; r0 < nbl; r0 += 4 * (kTopkThreads / 32)) {
+      const uint32_t r = r0 + grp;
+      const int64_t i0 = c0 + static_cast<int64_t>(r < nbl ? blist[r] : 0u) * 32 + (lane & 7u) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < nbl && i0 + 3 < c1) {
+        v = __ldg(reinterpret_cast<const float4*>(row + i0));
+      } else if (r < nbl) {
+        v.x = i0 + 0 < c1 ? __ldg(row + i0 + 0) : 0.0f;
+        v.y = i0 + 1 < c1 ? __ldg(row + i0 + 1) : 0.0f;
+        v.z = i0 + 2 < c1 ? __ldg(row + i0 + 2) : 0.0f;
+        v.w = i0 + 3 < c1 ? __ldg(row + i0 + 3) : 0.0f;
       }
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t msk = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        msk |= (r < nbl && i0 + j < c1 && (order_key(vv[j]) >> 21) >= bstar) ? (1u << j) : 0u;
+      warp_append(msk, &lctr[1], [&](uint32_t bit, uint32_t slot) {
+        const float x = bit == 0 ? v.x : (bit == 1 ? v.y : (bit == 2 ? v.z : v.w));
+        if (slot < kClLocalCap) lcand[slot] = make_uint2(order_key(x), static_cast<uint32_t>(i0 + bit));
+      });
+    }
+  } else {
+    // ---- pass 2 (keys): stage this chunk's entries above / in the threshold bin (the
+    // chunk is mostly still in L2)
+    for (int64_t base = c0; base < c1; base += 16 * kTopkThreads) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
+        if (i0 + 3 < c1) {
+          v[u] = __ldg(reinterpret_cast<const float4*>(row + i0));
+        } else {
+          v[u].x = i0 + 0 < c1 ? __ldg(row + i0 + 0) : 0.0f;
+          v[u].y = i0 + 1 < c1 ? __ldg(row + i0 + 1) : 0.0f;
+          v[u].z = i0 + 2 < c1 ? __ldg(row + i0 + 2) : 0.0f;
+          v[u].w = i0 + 3 < c1 ? __ldg(row + i0 + 3) : 0.0f;
+        }
+      }
+      uint32_t mhi = 0, meq = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
+        const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t bin = order_key(vv[j]) >> 21;
+          const bool in = i0 + j < c1;
+          mhi |= (in && bin > bstar) ? (1u << (4 * u + j)) : 0u;
+          meq |= (in && bin == bstar) ? (1u << (4 * u + j)) : 0u;
+        }
+      }
+      if (!__any_sync(0xffffffffu, (mhi | meq) != 0)) continue;
+      auto entry = [&](uint32_t bit, float& x) {
+        const int u = static_cast<int>(bit >> 2), j = static_cast<int>(bit & 3u);
+        const float4 w = u == 0 ? v[0] : (u == 1 ? v[1] : (u == 2 ? v[2] : v[3]));
+        x = j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
+        return base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4 + j;
+      };
+      warp_append(mhi, &lctr[0], [&](uint32_t bit, uint32_t slot) {
+        float x;
+        const int64_t idx = entry(bit, x);
+        if (slot < static_cast<uint32_t>(a.k)) lsel[slot] = static_cast<int32_t>(idx);
+      });
+      warp_append(meq, &lctr[1], [&](uint32_t bit, uint32_t slot) {
+        float x;
+        const int64_t idx = entry(bit, x);
+        if (slot < kClLocalCap) lcand[slot] = make_uint2(order_key(x), static_cast<uint32_t>(idx));
+      });
     }
   }
   __syncthreads();
+  // ---- hand the staged lists to the leader (one shared-cluster atomic per list)
   const uint32_t l_ctr = dsmem_map(&ctr[0], 0), l_sel = dsmem_map(sel, 0), l_cand = dsmem_map(cand, 0);
   const uint32_t n_hi = lctr[0] < static_cast<uint32_t>(a.k) ? lctr[0] : static_cast<uint32_t>(a.k);
   const uint32_t n_eq = lctr[1];
   if (threadIdx.x == 0) {
     s_base[0] = n_hi ? dsmem_atom_add(l_ctr, n_hi) : 0u;
     s_base[1] = n_eq ? dsmem_atom_add(l_ctr + 4u, n_eq) : 0u;
-    if (n_eq > kClLocalCap) dsmem_st(l_ctr + 12u, 1u);  // a staged list overflowed: the leader refines the row
+    if (n_eq > kClLocalCap || lctr[2] > static_cast<uint32_t>(kBins))
+      dsmem_st(l_ctr + 12u, 1u);  // a staged list overflowed: the leader selects over the whole row
   }
   __syncthreads();
   for (uint32_t i = threadIdx.x; i < n_hi; i += kTopkThreads)
@@ -607,72 +789,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(const TopkAr
     if (s_base[1] + i < kClCandCap) dsmem_st2(l_cand + 8u * (s_base[1] + i), lcand[i].x, lcand[i].y);
   cluster_sync_all();  // every hand-off has landed in the leader
   if (rank != 0) return;
-  // ---- leader: resolve the threshold bin exactly
-  const uint32_t above = s_above, nc = hsum[bstar], need = static_cast<uint32_t>(a.k) - above;
-  if (threadIdx.x == 0) {
-    if (ctr[0] != above || ctr[1] != nc) report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
-    ctr[2] = above;
-  }
-  __syncthreads();
-  uint32_t* hA = h;  // reuse this CTA's histogram as scratch
+  // ---- leader: exact selection among the candidates
+  const uint32_t above = by_blocks ? 0u : s_above;
+  const uint32_t nc = ctr[1];
+  if (!by_blocks && threadIdx.x == 0 && (ctr[0] != above || nc != hsum[bstar])) report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
   bool done = false;
-  if (nc <= kClCandCap && ctr[3] == 0) {
-    // level A: bits [10, 21) below the 11-bit prefix
-    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) hA[b] = 0;
+  if (ctr[3] == 0 && nc <= static_cast<uint32_t>(kClCandCap)) {
+    if (threadIdx.x == 0) ctr[2] = above;  // entries of higher bins are already in sel[0, above)
     __syncthreads();
-    for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) atomicAdd(&hA[(cand[i].x >> 10) & 0x7FFu], 1u);
-    __syncthreads();
-    threshold_bin(hA, need, &s_bin, &s_above, s_warp);
-    const uint32_t binA = static_cast<uint32_t>(s_bin), needA = need - s_above;
-    __syncthreads();
-    // level B: bits [0, 10) among the candidates of sub-bin binA
-    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) hA[b] = 0;
-    __syncthreads();
-    for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
-      const uint32_t key = cand[i].x;
-      if (((key >> 10) & 0x7FFu) == binA) atomicAdd(&hA[key & 0x3FFu], 1u);
-    }
-    __syncthreads();
-    threshold_bin(hA, needA, &s_bin, &s_above, s_warp);
-    const uint32_t binB = static_cast<uint32_t>(s_bin), needB = needA - s_above;
-    const uint32_t vstar = (bstar << 21) | (binA << 10) | binB;
-    const uint32_t n_ties = hA[binB];
-    __syncthreads();
-    if (n_ties <= kBins) {
-      // keys above vstar are chosen; ties at vstar are collected and the lowest indices taken
-      int32_t* ties = reinterpret_cast<int32_t*>(hsum);
-      if (threadIdx.x == 0) ctr[3] = 0;
-      __syncthreads();
-      for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
-        const uint2 c = cand[i];
-        if (c.x > vstar) sel[atomicAdd(&ctr[2], 1u)] = static_cast<int32_t>(c.y);
-        else if (c.x == vstar) ties[atomicAdd(&ctr[3], 1u)] = static_cast<int32_t>(c.y);
-      }
-      __syncthreads();
-      int p2 = 1;
-      while (p2 < static_cast<int>(n_ties)) p2 <<= 1;
-      for (int i = static_cast<int>(n_ties) + threadIdx.x; i < p2; i += kTopkThreads) ties[i] = 0x7FFFFFFF;
-      __syncthreads();
-      if (n_ties > 1) bitonic_sort(ties, p2);
-      const uint32_t base = above + (need - needB);
-      for (uint32_t i = threadIdx.x; i < needB; i += kTopkThreads) sel[base + i] = ties[i];
-      __syncthreads();
-      done = true;
-    }
+    done = select_candidates(cand, nc, static_cast<uint32_t>(a.k) - above, h, reinterpret_cast<int32_t*>(hsum), s_warp,
+                             sel, &ctr[2], &lctr[3]);
   }
-  if (!done) {
-    // massive ties or an overflowing hand-off: exact radix refinement over the whole row
-    if (threadIdx.x == 0) ctr[2] = above;
-    __syncthreads();
-    refine_row(a, q, nv, bstar, need, h, s_warp, sel, &ctr[2]);
-    __syncthreads();
-  }
+  if (!done) full_row_select(a, q, nv, h, s_warp, sel, &ctr[2]);
   sort_indices_out(threadIdx.x < a.k ? sel[threadIdx.x] : INT_MAX, reinterpret_cast<int32_t*>(hsum), out, a.k);
 }
 
 size_t topk_cluster_smem() {
   return 3 * kBins * sizeof(uint32_t) + 8 * sizeof(uint32_t) + 2 * 512 * sizeof(int32_t) +
-         (kClCandCap + kClLocalCap) * sizeof(uint2);
+         (kClCandCap + kClLocalCap) * sizeof(uint2) + kClBlockCap * sizeof(uint32_t);
 }
 
 cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream) {

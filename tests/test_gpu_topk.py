@@ -64,3 +64,18 @@ def test_topk_threshold_bin_crowded(orc, csa2):
     t = 50000
     S = (1.0 + g.random((2, t)) * 0.2).astype(np.float32)
     _check(orc, csa2, S, [t, 30000])
+
+
+def test_topk_long_rows_block_bound(orc, csa2):
+    # long rows select through the 32-entry block-maximum lower bound; one 1M-entry row
+    lens = [131072, 131072, 262144, 1048576]
+    _check(orc, csa2, _rows(5, lens, max(lens)), lens)
+
+
+def test_topk_increasing_rows_overflow_to_whole_row(orc, csa2):
+    # increasing scores make the block bound as loose as it gets (every entry of the last
+    # 512 blocks is a candidate): the staged lists overflow and the leader selects over
+    # the whole row; exact ties across blocks ride along
+    t = 60000
+    S = np.stack([np.arange(t, dtype=np.float32), np.repeat(np.arange(t // 40, dtype=np.float32), 40)[:t]])
+    _check(orc, csa2, S, [t, t])
