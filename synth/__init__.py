@@ -107,3 +107,21 @@ def torch_distinct_indices(seed: int, n_queries: int, n_visible: int, k: int, de
         perm = torch.randperm(u.numel(), generator=g, device=device)[:k]
         out[q] = u[perm].to(torch.int32)
     return out
+
+
+def torch_normal_bf16_rows_with_outliers(seed: int, n: int, width: int, frac: float, factor: float, device):
+    """Device twin of the row recipe above: [n][width] N(0,1) rows drawn directly in bf16
+    with a seeded torch.Generator (the generator rounds each draw to nearest),
+    round(frac*n) distinct rows (a seeded permutation's prefix) multiplied by `factor`
+    (a power of two: exact in bf16)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.randn((n, width), generator=g, device=device, dtype=torch.bfloat16)
+    m = int(round(frac * n))
+    if m:
+        g2 = torch.Generator(device=device)
+        g2.manual_seed(int(seed) + 7919)
+        rows = torch.randperm(n, generator=g2, device=device)[:m]
+        x[rows] *= float(factor)
+    return x
