@@ -81,6 +81,28 @@ struct AttnArgs {
 
 using TraceFn = void (*)(int, cudaStream_t);
 
+// Launches `kernel` so that it may start while the previous kernel on the stream
+// drains (programmatic stream serialization); the kernel must call pdl_wait() before
+// touching the previous kernel's outputs or anything it reads.  extra: an optional
+// further launch attribute (a cluster shape).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       const cudaLaunchAttribute* extra, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (extra != nullptr) attr[n++] = *extra;
+  cfg.attrs = attr;
+  cfg.numAttrs = static_cast<unsigned>(n);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t stream);
 size_t index_smem_bytes(int stages);
 cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream);

@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  pdl_trigger();
+  pdl_wait();  // the selected indices (and in Full mode the new entries) come from earlier kernels
   // queries of this CTA's heads, then the window rows, -> shared memory (operand
   // layout, K-major over the 512 channels); two cp.async groups
   {
@@ -410,8 +412,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
   static std::atomic<int> limit_set[kMaxDevices];
   cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(attn_kernel), smem, limit_set);
   if (e != cudaSuccess) return e;
-  attn_kernel<<<static_cast<unsigned>(2 * a.n_q), kAttnThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_kernel, dim3(static_cast<unsigned>(2 * a.n_q)), dim3(kAttnThreads), smem, stream, nullptr, a);
 }
 
 }  // namespace csa2

@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  pdl_trigger();
+  pdl_wait();  // the packed query groups and new cache entries come from the previous kernel
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -370,8 +372,7 @@ cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream) {
   static std::atomic<int> limit_set[kMaxDevices];
   cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(index_kernel), smem, limit_set);
   if (e != cudaSuccess) return e;
-  index_kernel<<<grid, kIdxThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(index_kernel, dim3(static_cast<unsigned>(grid)), dim3(kIdxThreads), smem, stream, nullptr, a);
 }
 
 }  // namespace csa2

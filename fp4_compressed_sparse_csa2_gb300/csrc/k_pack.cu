@@ -30,6 +30,8 @@ __device__ __forceinline__ void load16(const __nv_bfloat16* src, float (&x)[16])
 // entry); items [n_new*40, +n_groups*128*8) pack indexer-query rows (rows >= N of a
 // group only clear their scale bytes).
 __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
+  pdl_trigger();
+  pdl_wait();  // the previous step's kernels may still read the cache slots written here
   const int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t n_pack = a.n_new * 40;
   if (item < n_pack) {
@@ -92,8 +94,7 @@ cudaError_t launch_pack(const PackArgs& a, cudaStream_t stream) {
   const int64_t items = a.n_new * 40 + a.n_groups * 128 * 8;
   if (items == 0) return cudaSuccess;
   const int64_t blocks = (items + 255) / 256;
-  pack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(pack_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, nullptr, a);
 }
 
 }  // namespace csa2

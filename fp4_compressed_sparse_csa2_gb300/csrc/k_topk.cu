@@ -610,6 +610,8 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
   __shared__ int s_bin;
   __shared__ uint32_t s_above;
   __shared__ uint32_t s_base[2];
+  pdl_trigger();
+  pdl_wait();  // the score rows come from the previous kernel
   const uint32_t rank = cluster_rank();
   const uint32_t csize = gridDim.x;  // one cluster spans the x dimension
   const uint32_t lane = threadIdx.x & 31;
@@ -854,9 +856,9 @@ cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t st
   (void)sm_count;
   int64_t chunk = (a.t_max + c - 1) / c;
   chunk = ((chunk + 2047) / 2048) * 2048;
-  cfg.gridDim = dim3(static_cast<unsigned>(c), static_cast<unsigned>(a.n_q), 1);
   attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a, chunk);
+  return launch_pdl(topk_cluster_kernel, dim3(static_cast<unsigned>(c), static_cast<unsigned>(a.n_q), 1),
+                    dim3(kTopkThreads), smem, stream, &attr[0], a, chunk);
 }
 
 }  // namespace csa2
