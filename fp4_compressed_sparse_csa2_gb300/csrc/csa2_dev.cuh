@@ -65,6 +65,30 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+// Order-preserving 32-bit key of an fp32 score (larger score -> larger key; -0 and +0
+// share one key; a real score never has key 0).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0u) u = 0u;  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Maximum of v over the full warp (every lane must take part).
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// The smallest fp32 value whose order key is at least `key` (key 0x80000000 gives +0;
+// keys at or below the key of -inf give -inf).  v >= key_floor(k) exactly when
+// order_key(v) >= k, for every non-NaN v.
+__device__ __forceinline__ float key_floor(uint32_t key) {
+  if (key & 0x80000000u) return __uint_as_float(key & 0x7FFFFFFFu);
+  const float f = __uint_as_float(~key);
+  return f != f ? -INFINITY : f;  // below -inf's key lie only negative NaN patterns
+}
+
 // Programmatic dependent launch.  pdl_wait() returns once the previous kernel on the
 // stream has completed and its memory is visible (immediately when the launch did not
 // overlap it); every kernel calls it before touching that kernel's outputs or anything

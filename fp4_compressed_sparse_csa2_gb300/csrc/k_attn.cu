@@ -58,11 +58,6 @@ __device__ __forceinline__ void cp_async16(uint32_t sdst, const void* gsrc, uint
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__device__ __forceinline__ float redux_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
 
 // E4M3 code -> bf16 (exact: 4 significant bits, range 2^-9 .. 448), both halves.
 __device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
@@ -115,7 +110,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     tmem_relinquish();
   }
   pdl_trigger();
-  pdl_wait();  // the selected indices (and in Full mode the new entries) come from earlier kernels
   // queries of this CTA's heads, then the window rows, -> shared memory (operand
   // layout, K-major over the 512 channels); two cp.async groups
   {
@@ -137,6 +131,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     }
     cp_async_commit();
   }
+  // The copies above read only this call's inputs, so they overlap the previous kernel's
+  // tail; the selected indices (and in Full mode the new entries) come from earlier kernels.
+  pdl_wait();
   // offsets of the 512 selected records (one round trip for all indices)
   if (tid < 4) tile_cnt[tid] = 0;
   __syncthreads();

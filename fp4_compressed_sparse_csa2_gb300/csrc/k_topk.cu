@@ -28,11 +28,6 @@ constexpr int kChunk = 8192;  // score entries per CTA in the hist and select pa
 constexpr int kCandCap = 4096;
 constexpr int kTopkThreads = 512;
 
-__device__ __forceinline__ uint32_t order_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if ((u << 1) == 0u) u = 0u;  // -0 -> +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 __device__ __forceinline__ int64_t row_visible(const TopkArgs& a, int64_t q) {
   int64_t nv = __ldg(a.n_visible + q);
@@ -507,9 +502,14 @@ __device__ bool select_candidates(const uint2* cand, uint32_t nc, uint32_t need,
     const int sh = shifts[lv], wd = widths[lv];
     for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
     __syncthreads();
-    for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
-      const uint32_t key = cand[i].x;
-      if (pbits == 0 || (key >> (32 - pbits)) == prefix) atomicAdd(&h[(key >> sh) & ((1u << wd) - 1u)], 1u);
+    for (uint32_t base = 0; base < nc; base += kTopkThreads) {
+      const uint32_t i = base + threadIdx.x;
+      const uint32_t key = i < nc ? cand[i].x : 0u;
+      const bool in = i < nc && (pbits == 0 || (key >> (32 - pbits)) == prefix);
+      const uint32_t bin = in ? (key >> sh) & ((1u << wd) - 1u) : 0xFFFFFFFFu;
+      // candidates crowd a few bins: one atomic per distinct bin of the warp
+      const uint32_t same = __match_any_sync(0xffffffffu, bin);
+      if (in && (threadIdx.x & 31) == static_cast<uint32_t>(__ffs(same) - 1)) atomicAdd(&h[bin], __popc(same));
     }
     __syncthreads();
     threshold_bin(h, need_l, &s_bin, &s_above, s_warp);
@@ -592,6 +592,62 @@ __device__ __forceinline__ void warp_append(uint32_t msk, uint32_t* counter, Emi
     emit(bit, slot);
     ++slot;
     msk &= msk - 1u;
+  }
+}
+
+// Stages the keys of bin >= bstar from the listed 32-entry blocks of row[c0, c1): 8
+// lanes per block, 4 blocks per warp and kRounds such groups of loads in flight per lane;
+// (key, index) pairs go to cand[0, cap) through one packed warp scan per append
+// (*counter counts every pair, also those beyond cap).
+template <uint32_t kRounds>
+__device__ __forceinline__ void gather_block_candidates(const float* row, int64_t c0, int64_t c1, const uint32_t* blist,
+                                                        uint32_t nbl, uint32_t bstar, uint2* cand, uint32_t cap,
+                                                        uint32_t* counter) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5, grp = lane >> 3;
+  constexpr uint32_t kStride = 4 * (kTopkThreads / 32);
+  for (uint32_t r0 = warp * 4; r0 < nbl; r0 += kRounds * kStride) {
+    float4 v[kRounds];
+    int64_t i0[kRounds];
+    bool ok[kRounds];
+#pragma unroll
+    for (uint32_t u = 0; u < kRounds; ++u) {
+      const uint32_t r = r0 + u * kStride + grp;
+      ok[u] = r < nbl;
+      i0[u] = c0 + static_cast<int64_t>(ok[u] ? blist[r] : 0u) * 32 + (lane & 7u) * 4;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok[u] && i0[u] + 3 < c1) {
+        v[u] = __ldg(reinterpret_cast<const float4*>(row + i0[u]));
+      } else if (ok[u]) {
+        v[u].x = i0[u] + 0 < c1 ? __ldg(row + i0[u] + 0) : 0.0f;
+        v[u].y = i0[u] + 1 < c1 ? __ldg(row + i0[u] + 1) : 0.0f;
+        v[u].z = i0[u] + 2 < c1 ? __ldg(row + i0[u] + 2) : 0.0f;
+        v[u].w = i0[u] + 3 < c1 ? __ldg(row + i0[u] + 3) : 0.0f;
+      }
+    }
+    // kRounds <= 8: 4 entries per round fit the 32-bit mask; bin >= b* is a plain float
+    // comparison with the bin's lower edge
+    const float lo = key_floor(bstar << 21);
+    uint32_t msk = 0;
+#pragma unroll
+    for (uint32_t u = 0; u < kRounds; ++u) {
+      const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) msk |= (ok[u] && i0[u] + j < c1 && vv[j] >= lo) ? (1u << (4 * u + j)) : 0u;
+    }
+    if (!__any_sync(0xffffffffu, msk != 0)) continue;
+    warp_append(msk, counter, [&](uint32_t bit, uint32_t slot) {
+      const uint32_t u = bit >> 2, j = bit & 3u;
+      float4 w = v[0];
+      int64_t b = i0[0];
+#pragma unroll
+      for (uint32_t x = 1; x < kRounds; ++x)
+        if (u == x) {
+          w = v[x];
+          b = i0[x];
+        }
+      const float e = j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
+      if (slot < cap) cand[slot] = make_uint2(order_key(e), static_cast<uint32_t>(b + j));
+    });
   }
 }
 
@@ -700,29 +756,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
     }
     __syncthreads();
     const uint32_t nbl = lctr[2] < static_cast<uint32_t>(kBins) ? lctr[2] : static_cast<uint32_t>(kBins);
-    const uint32_t warp = threadIdx.x >> 5, grp = lane >> 3;
-    for (uint32_t r0 = warp * 4; r0 < nbl; r0 += 4 * (kTopkThreads / 32)) {
-      const uint32_t r = r0 + grp;
-      const int64_t i0 = c0 + static_cast<int64_t>(r < nbl ? blist[r] : 0u) * 32 + (lane & 7u) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < nbl && i0 + 3 < c1) {
-        v = __ldg(reinterpret_cast<const float4*>(row + i0));
-      } else if (r < nbl) {
-        v.x = i0 + 0 < c1 ? __ldg(row + i0 + 0) : 0.0f;
-        v.y = i0 + 1 < c1 ? __ldg(row + i0 + 1) : 0.0f;
-        v.z = i0 + 2 < c1 ? __ldg(row + i0 + 2) : 0.0f;
-        v.w = i0 + 3 < c1 ? __ldg(row + i0 + 3) : 0.0f;
-      }
-      const float vv[4] = {v.x, v.y, v.z, v.w};
-      uint32_t msk = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        msk |= (r < nbl && i0 + j < c1 && (order_key(vv[j]) >> 21) >= bstar) ? (1u << j) : 0u;
-      warp_append(msk, &lctr[1], [&](uint32_t bit, uint32_t slot) {
-        const float x = bit == 0 ? v.x : (bit == 1 ? v.y : (bit == 2 ? v.z : v.w));
-        if (slot < kClLocalCap) lcand[slot] = make_uint2(order_key(x), static_cast<uint32_t>(i0 + bit));
-      });
-    }
+    gather_block_candidates<4>(row, c0, c1, blist, nbl, bstar, lcand, kClLocalCap, &lctr[1]);
   } else {
     // ---- pass 2 (keys): stage this chunk's entries above / in the threshold bin (the
     // chunk is mostly still in L2)
@@ -860,5 +894,6 @@ cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t st
   return launch_pdl(topk_cluster_kernel, dim3(static_cast<unsigned>(c), static_cast<unsigned>(a.n_q), 1),
                     dim3(kTopkThreads), smem, stream, &attr[0], a, chunk);
 }
+
 
 }  // namespace csa2
