@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before timing (clock sampling)")
+    p.add_argument("--no-extra", action="store_true", help="skip the other workloads (tiny, Reuse/Reindex, 1M, prefill)")
     return p.parse_args()
 
 
@@ -269,6 +270,181 @@ def profiled_traffic(summary: str, sources, entries: int):
     return int(round(per_entry * entries))
 
 
+
+# ----------------------------------------------------------------------------- other workloads
+def _device_cache(csa2, dev, n_req, n_entries, max_pages, seed, frac=0.0):
+    """A paged cache of n_req requests x n_entries seeded entries, packed by the library."""
+    import synth
+    n_pages = n_req * max_pages
+    kv = torch.empty(n_pages * csa2.KV_PAGE_BYTES, dtype=torch.uint8, device=dev)
+    idx = torch.empty(n_pages * csa2.IDX_PAGE_BYTES, dtype=torch.uint8, device=dev)
+    cache = csa2.make_cache(kv, idx, max_pages)
+    ws0 = csa2.alloc_workspace(1, 64, 0, False, dev)
+    pos = torch.arange(n_entries, dtype=torch.int64, device=dev)
+    for r in range(n_req):
+        lat = synth.torch_normal_bf16_rows_with_outliers(seed + r, n_entries, D, frac, 8.0, dev)
+        key = synth.torch_normal_bf16_rows_with_outliers(seed + r + 50000, n_entries, DI, frac, 8.0, dev)
+        csa2.pack_kv(lat, key, torch.full((n_entries,), r, dtype=torch.int32, device=dev), pos, cache, ws0)
+        del lat, key
+    torch.cuda.synchronize()
+    return cache
+
+
+def _timed(csa2, fn, warmup, steps):
+    """ms per call with CUDA events on the launching stream, then per-kernel device times
+    from a second, traced pass."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    csa2.trace_enable(True)
+    for _ in range(steps):
+        fn()
+    torch.cuda.synchronize()
+    kernels = {}
+    for k in csa2.TRACE_KINDS:
+        tot, n = csa2.trace_read(k)
+        if n:
+            kernels[k] = round(1000 * tot / n, 2)
+    csa2.trace_enable(False)
+    return ms, kernels
+
+
+def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3):
+    import synth
+    mp = (T + 127) // 128
+    cache = _device_cache(csa2, dev, B, T - 1, mp, seed, frac)
+    sb = seed + 7_000_000
+    q = synth.torch_normal_bf16(sb + 1, (B, HEADS, D), dev)
+    q_idx = synth.torch_normal_bf16(sb + 2, (B, HEADS_I, DI), dev)
+    w = synth.torch_normal_f32(sb + 3, (B, HEADS_I), dev)
+    new_lat = synth.torch_normal_bf16(sb + 4, (B, D), dev)
+    new_key = synth.torch_normal_bf16(sb + 5, (B, DI), dev)
+    window = synth.torch_normal_bf16(sb + 6, (B * WIN, D), dev)
+    out = torch.empty((B, HEADS, D), dtype=torch.bfloat16, device=dev)
+    step = csa2.make_step(n_q=B, t_max=T, q=q, req=torch.arange(B, dtype=torch.int32, device=dev),
+                          n_visible=torch.full((B,), T, dtype=torch.int32, device=dev), window=window,
+                          win_start=torch.arange(B, dtype=torch.int64, device=dev) * WIN,
+                          win_len=torch.full((B,), WIN, dtype=torch.int32, device=dev), cache=cache,
+                          topk_idx=torch.empty((B, TOPK), dtype=torch.int32, device=dev), out=out,
+                          lse=torch.empty((B, HEADS), dtype=torch.float32, device=dev), q_idx=q_idx, w=w,
+                          heads_I=HEADS_I, group=1, n_new=B, new_latent=new_lat, new_idx_key=new_key,
+                          new_req=torch.arange(B, dtype=torch.int32, device=dev),
+                          new_pos=torch.full((B,), T - 1, dtype=torch.int64, device=dev))
+    ws = csa2.alloc_workspace(B, HEADS_I, T, True, dev)
+    ms, kernels = _timed(csa2, lambda: csa2.sparse_attn_full(step, ws), warmup, steps)
+    st, info = csa2.check(ws)
+    must = B * (T * 72 + TOPK * 288 + WIN * D * 2)
+    return {"workload": name, "metric": UNIT, "value": round(1000.0 / ms, 2), "ms_per_step": round(ms, 4),
+            "must_read_bytes": must, "step_gbs": round(must / (ms * 1e-3) / 1e9, 1),
+            "index_gbs": round(B * T * 72 / (kernels.get("index", float("nan")) * 1e-6) / 1e9, 1),
+            "kernels_us": kernels, "device_status": st}
+
+
+def measure_extra(dev, hbm_peak, bf16_tflops):
+    """The other workloads of the layer, each in its own line: the tiny decode, Reuse and
+    Reindex at 128 x 262,144, the million-token decode with its ratio-2 layer (1 % of
+    entries x 8), and a 4,096-token chunked prefill on 262,144 cached entries."""
+    import synth
+    from fp4_compressed_sparse_csa2_gb300 import csa2
+    lines = []
+
+    def attempt(fn):
+        try:
+            lines.append(fn())
+        except Exception as exc:  # a failed extra workload is reported, the headline stands
+            lines.append({"error": f"{type(exc).__name__}: {exc}"[:300]})
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    attempt(lambda: dict(_decode_line(csa2, dev, "tiny Full decode, B=1, T=4096 (L2-resident)", 1, 4096, 0),
+                         note="launch-latency bound"))
+
+    def reuse_reindex():
+        B, T = 128, 262144
+        mp = T // 128
+        cache = _device_cache(csa2, dev, B, T, mp, 2000)
+        q = synth.torch_normal_bf16(2000 + 7_000_001, (B, HEADS, D), dev)
+        window = synth.torch_normal_bf16(2000 + 7_000_006, (B * WIN, D), dev)
+        common = dict(n_q=B, t_max=T, q=q, req=torch.arange(B, dtype=torch.int32, device=dev),
+                      n_visible=torch.full((B,), T, dtype=torch.int32, device=dev), window=window,
+                      win_start=torch.arange(B, dtype=torch.int64, device=dev) * WIN,
+                      win_len=torch.full((B,), WIN, dtype=torch.int32, device=dev), cache=cache,
+                      out=torch.empty((B, HEADS, D), dtype=torch.bfloat16, device=dev),
+                      lse=torch.empty((B, HEADS), dtype=torch.float32, device=dev))
+        sel = synth.torch_distinct_indices(2000 + 7_000_007, B, T, TOPK, dev)
+        ws = csa2.alloc_workspace(B, HEADS_I, T, True, dev)
+        reuse = csa2.make_step(topk_idx=sel, **common)
+        ms_u, k_u = _timed(csa2, lambda: csa2.sparse_attn_reuse(reuse, ws), 3, 20)
+        reidx = csa2.make_step(topk_idx=torch.empty((B, TOPK), dtype=torch.int32, device=dev),
+                               q_idx=synth.torch_normal_bf16(2000 + 7_000_002, (B, HEADS_I, DI), dev),
+                               w=synth.torch_normal_f32(2000 + 7_000_003, (B, HEADS_I), dev), heads_I=HEADS_I,
+                               **common)
+        ms_r, k_r = _timed(csa2, lambda: csa2.sparse_attn_reindex(reidx, ws), 3, 10)
+        st, _ = csa2.check(ws)
+        must_u = B * (TOPK * 288 + WIN * D * 2)
+        must_r = B * (T * 72) + must_u
+        return {"workload": "Reuse and Reindex decode, B=128, T=262144", "metric": UNIT,
+                "reuse": {"value": round(1000.0 / ms_u, 2), "ms_per_step": round(ms_u, 4), "kernels_us": k_u,
+                          "must_read_bytes": must_u, "step_gbs": round(must_u / (ms_u * 1e-3) / 1e9, 1)},
+                "reindex": {"value": round(1000.0 / ms_r, 2), "ms_per_step": round(ms_r, 4), "kernels_us": k_r,
+                            "must_read_bytes": must_r, "step_gbs": round(must_r / (ms_r * 1e-3) / 1e9, 1),
+                            "index_gbs": round(B * T * 72 / (k_r.get("index", float("nan")) * 1e-6) / 1e9, 1)},
+                "device_status": st}
+
+    attempt(reuse_reindex)
+    attempt(lambda: dict(_decode_line(csa2, dev, "million-token Full decode, B=8, T=1048576, 1% of entries x8", 8,
+                                      1 << 20, 3000, 0.01), note="decoder layer"))
+    attempt(lambda: dict(_decode_line(csa2, dev, "ratio-2 layer Full decode, B=8, 524288 pooled entries, 1% x8", 8,
+                                      1 << 19, 3100, 0.01), note="encoder-style layer of the same step"))
+
+    def prefill():
+        n0, n = 262144, 4096
+        T = n0 + n
+        mp = T // 128
+        cache = _device_cache(csa2, dev, 1, n0, mp, 4000)
+        sb = 4000 + 7_000_000
+        new_lat = synth.torch_normal_bf16(sb + 4, (n, D), dev)
+        new_key = synth.torch_normal_bf16(sb + 5, (n, DI), dev)
+        rows = torch.cat([synth.torch_normal_bf16(sb + 6, (127, D), dev), new_lat]).contiguous()
+        step = csa2.make_step(n_q=n, t_max=T, q=synth.torch_normal_bf16(sb + 1, (n, HEADS, D), dev),
+                              req=torch.zeros(n, dtype=torch.int32, device=dev),
+                              n_visible=torch.arange(n0 + 1, T + 1, dtype=torch.int32, device=dev), window=rows,
+                              win_start=torch.arange(n, dtype=torch.int64, device=dev),
+                              win_len=torch.full((n,), WIN, dtype=torch.int32, device=dev), cache=cache,
+                              topk_idx=torch.empty((n, TOPK), dtype=torch.int32, device=dev),
+                              out=torch.empty((n, HEADS, D), dtype=torch.bfloat16, device=dev),
+                              lse=torch.empty((n, HEADS), dtype=torch.float32, device=dev),
+                              q_idx=synth.torch_normal_bf16(sb + 2, (n, HEADS_I, DI), dev),
+                              w=synth.torch_normal_f32(sb + 3, (n, HEADS_I), dev), heads_I=HEADS_I, group=2,
+                              n_new=n, new_latent=new_lat, new_idx_key=new_key,
+                              new_req=torch.zeros(n, dtype=torch.int32, device=dev),
+                              new_pos=torch.arange(n0, T, dtype=torch.int64, device=dev))
+        ws = csa2.alloc_workspace(n, HEADS_I, T, True, dev)
+        ms, kernels = _timed(csa2, lambda: csa2.sparse_attn_full(step, ws), 2, 5)
+        st, _ = csa2.check(ws)
+        pairs = n * n0 + n * (n + 1) // 2                 # visible (query, entry) pairs
+        flops = pairs * HEADS_I * DI * 2
+        fp4_peak = bf16_tflops * 6.0                      # 13.5 / 2.25 nominal ratio
+        idx_tf = flops / (kernels.get("index", float("nan")) * 1e-6) / 1e12
+        return {"workload": "chunked prefill: 4096 new tokens on 262144 cached entries, index groups of 2",
+                "metric": "chunk-steps/s", "value": round(1000.0 / ms, 3), "ms_per_step": round(ms, 3),
+                "kernels_us": kernels, "index_tflops": round(idx_tf, 1),
+                "index_fp4_frac": round(idx_tf / fp4_peak, 4),
+                "fp4_peak_tflops": round(fp4_peak, 1),
+                "fp4_peak_source": "measured bf16 burst x 6 (the nominal fp4/bf16 dense ratio)",
+                "index_flops": flops, "device_status": st}
+
+    attempt(prefill)
+    return lines
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -386,6 +562,9 @@ def run_ours(args, ws, rank, local):
                          f"threads, scaled to one {wl.B}-request layer-step"}
 
     clocks = clk.summary()
+    extra = None
+    if rank == 0 and ws == 1 and not args.no_extra:
+        extra = measure_extra(dev, hbm_peak, float(peaks.get("bf16_tflops", 1900.0)))
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -404,6 +583,7 @@ def run_ours(args, ws, rank, local):
                         for k, v in kernels.items()},
             "gpu_launches": int(launches),
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+            "extra": extra,
         }
         print(json.dumps(line), flush=True)
 

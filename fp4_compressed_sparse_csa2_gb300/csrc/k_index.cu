@@ -69,6 +69,8 @@ __device__ __forceinline__ int64_t seg_page(const Segment& sg, int32_t t) {
   return sg.bt_row ? static_cast<int64_t>(__ldg(sg.bt_row + t)) : sg.page_base + t;
 }
 
+// kSplit: N = 128 (two queries of 64 heads per group), handled by warpgroup pairs.
+template <bool kSplit>
 __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -96,7 +98,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
   // run two barrier phases ahead (parity waits would alias): the active issuer and
   // warpgroup counts divide n_acc.
   const uint32_t n_iss = kIssuers < static_cast<uint32_t>(n_acc) ? kIssuers : static_cast<uint32_t>(n_acc);
-  const uint32_t n_wg = kEpiGroups < static_cast<uint32_t>(n_acc) ? kEpiGroups : static_cast<uint32_t>(n_acc);
+  // N <= 64: warpgroup w serves accumulator w.  N = 128 (two queries of 64 heads): the
+  // four warpgroups pair up, warpgroup w reads the 64 columns (one query) w >> 1 of
+  // accumulator w & 1, so both accumulators keep two warpgroups busy.
+  constexpr bool split_cols = kSplit;
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);       // the producer's one arrive per stage (plus the copies' bytes)
@@ -104,7 +109,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], split_cols ? 256 : 128);  // every reader of the accumulator
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
@@ -277,8 +282,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // warpgroup wg takes the tiles with n % n_wg == wg; thread = TMEM lane = key
+    // thread = TMEM lane = key.  N <= 64: warpgroup wg takes the tiles with n % 4 == wg
+    // and every column; N = 128: the tiles with n % 2 == wg % 2 and the 64 columns (the
+    // query) wg / 2.
     const uint32_t wg = static_cast<uint32_t>(warp - 1 - kIssuers) >> 2;
+    const uint32_t wg_step = split_cols ? 2u : 4u, wg_res = split_cols ? (wg & 1u) : wg;
+    const uint32_t c_lo = split_cols ? 64u * (wg >> 1) : 0u, c_hi = split_cols ? c_lo + 64u : N;
     const int quarter = warp & 3;
     // one leader warp per warpgroup polls the accumulator barrier; the other three park
     // on a named barrier and cost no issue slots while they wait
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     uint32_t n = 0, own = 0;
     bool ok = true;
     Segment sg;
-    for (int64_t g = g_first; ok && wg < n_wg && g <= g_last; ++g) {
+    for (int64_t g = g_first; ok && g <= g_last; ++g) {
       if (!segment(a, g, begin, end, sg)) continue;
       const int64_t q0 = g * a.G;
       __syncwarp();
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
       __syncwarp();
       const int nq = static_cast<int>(a.n_q - q0 < a.G ? a.n_q - q0 : a.G);
       const uint32_t len = static_cast<uint32_t>(sg.t1 - sg.t0);
-      for (uint32_t nn = n + ((wg - n) & (n_wg - 1u)); nn < n + len; nn += n_wg) {
+      for (uint32_t nn = n + ((wg_res - n) & (wg_step - 1u)); nn < n + len; nn += wg_step) {
         const int32_t t = sg.t0 + static_cast<int32_t>(nn - n);
         const uint32_t bb = nn & static_cast<uint32_t>(n_acc - 1);
         const uint32_t bp = (nn >> (n_acc == 4 ? 2 : 1)) & 1u;
@@ -323,11 +332,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         const uint32_t hmask = static_cast<uint32_t>(a.heads_I) - 1u;
         const uint32_t lg_h = a.heads_I == 64 ? 6u : 5u;
         float2 acc01 = make_float2(0.0f, 0.0f), acc23 = make_float2(0.0f, 0.0f);
-        for (uint32_t c = 0; c < N; c += 32u) {
+        for (uint32_t c = c_lo; c < c_hi; c += 32u) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + bb * N + c, r);
           tmem_ld_wait();
-          if (c + 32u >= N) {
+          if (c + 32u >= c_hi) {
             tc_fence_before();
             mbar_arrive(&acc_empty[bb]);
           }
@@ -369,10 +378,12 @@ size_t index_smem_bytes(int stages) {
 
 cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream) {
   const size_t smem = index_smem_bytes(a.stages);
-  static std::atomic<int> limit_set[kMaxDevices];
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(index_kernel), smem, limit_set);
+  static std::atomic<int> limit_set[2][kMaxDevices];
+  const bool split = a.N == 128;
+  auto* kernel = split ? index_kernel<true> : index_kernel<false>;
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kernel), smem, limit_set[split ? 1 : 0]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(index_kernel, dim3(static_cast<unsigned>(grid)), dim3(kIdxThreads), smem, stream, nullptr, a);
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kIdxThreads), smem, stream, nullptr, a);
 }
 
 }  // namespace csa2

@@ -405,7 +405,7 @@ cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes) {
 namespace csa2 {
 
 constexpr int kClCandCap = 4096;   // leader: candidates of the threshold bin
-constexpr int kClLocalCap = 1024;  // per CTA: staged candidates of the threshold bin
+constexpr int kClLocalCap = 4096;  // per CTA: staged candidates (long rows on 2-CTA clusters stage ~1.5 K)
 constexpr int kClBlockCap = 4096;  // per CTA: block maxima (32-entry blocks) of the chunk
 
 __device__ __forceinline__ uint32_t cluster_rank() {
