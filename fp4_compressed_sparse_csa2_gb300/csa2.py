@@ -45,7 +45,8 @@ class csa2_step(ctypes.Structure):
                 ("new_latent", ctypes.c_void_p), ("new_idx_key", ctypes.c_void_p), ("new_req", ctypes.c_void_p),
                 ("new_pos", ctypes.c_void_p), ("cache", csa2_cache), ("topk_idx", ctypes.c_void_p),
                 ("scores", ctypes.c_void_p), ("ld", ctypes.c_int64), ("softmax_scale", ctypes.c_float),
-                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("sinks", ctypes.c_void_p),
+                ("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p)]
 
 
 def _load():
@@ -135,13 +136,15 @@ def topk_noalloc(scores, ld, n_visible, n_q, t_max, k, out_idx, stream=None):
 
 def make_step(*, n_q, t_max, q, req, n_visible, window, win_start, win_len, cache, topk_idx, out, q_idx=None,
               w=None, heads_I=64, group=1, n_new=0, new_latent=None, new_idx_key=None, new_req=None, new_pos=None,
-              scores=None, ld=0, softmax_scale=0.0, lse=None) -> csa2_step:
+              scores=None, ld=0, softmax_scale=0.0, lse=None, sinks=None, rope_cos=None,
+              rope_sin=None) -> csa2_step:
     s = csa2_step(int(n_q), HEADS, int(heads_I), TOPK, int(group), int(t_max), _ptr(q), _ptr(q_idx), _ptr(w),
                   _ptr(req), _ptr(n_visible), _ptr(window), _ptr(win_start), _ptr(win_len), int(n_new),
                   _ptr(new_latent), _ptr(new_idx_key), _ptr(new_req), _ptr(new_pos), cache, _ptr(topk_idx),
-                  _ptr(scores), int(ld), float(softmax_scale), _ptr(out), _ptr(lse))
+                  _ptr(scores), int(ld), float(softmax_scale), _ptr(out), _ptr(lse), _ptr(sinks), _ptr(rope_cos),
+                  _ptr(rope_sin))
     s._keep = (q, req, n_visible, window, win_start, win_len, cache, topk_idx, out, q_idx, w, new_latent,
-               new_idx_key, new_req, new_pos, scores, lse)
+               new_idx_key, new_req, new_pos, scores, lse, sinks, rope_cos, rope_sin)
     return s
 
 

@@ -244,6 +244,9 @@ csa2_status run_attn(const csa2_step& s, int32_t* err, cudaStream_t stream) {
   a.lse = s.lse;
   a.n_q = s.n_q;
   a.err = err;
+  a.sinks = s.sinks;
+  a.rope_cos = s.rope_cos;
+  a.rope_sin = s.rope_sin;
   trace_begin(kAttn, stream);
   const cudaError_t e = launch_attn(a, stream);
   trace_end(kAttn, stream);
@@ -264,6 +267,8 @@ csa2_status check_step(const csa2_step* s, Mode mode) {
     if (!s->window || !aligned(s->window, 16) || !s->win_start || !s->win_len)
       return fail(CSA2_ERR_INVALID_ARG, "window, win_start and win_len are required (window 16-byte aligned)");
     if (!s->topk_idx) return fail(CSA2_ERR_INVALID_ARG, "topk_idx is NULL");
+    if ((s->rope_cos == nullptr) != (s->rope_sin == nullptr))
+      return fail(CSA2_ERR_INVALID_ARG, "rope_cos and rope_sin go together");
   }
   if (s->t_max < 0 || s->t_max > static_cast<int64_t>(s->cache.max_pages) * kPage)
     return fail(CSA2_ERR_INVALID_ARG, "t_max %lld outside [0, max_pages*128]", static_cast<long long>(s->t_max));

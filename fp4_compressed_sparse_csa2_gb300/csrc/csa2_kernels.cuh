@@ -77,6 +77,9 @@ struct AttnArgs {
   float* lse;
   int64_t n_q;
   int32_t* err;
+  const float* sinks;     // [64] natural-log sink logits or nullptr
+  const float* rope_cos;  // [n_q][32] or nullptr (then rope_sin too)
+  const float* rope_sin;
 };
 
 using TraceFn = void (*)(int, cudaStream_t);

@@ -23,6 +23,11 @@
 //   O^T      32 tcgen05.mma (4 M-tiles of 128 output channels, N = 32 heads, K = 128
 //            keys) reading the SAME bf16 tile as an MN-major operand (K == V);
 //   epilogue O = O^T / l per head -> bf16, lse = ln(sum exp).
+// Optional, from "From MLA to DSA to HCA/CSA": per-head attention sinks (a logit that
+// joins the softmax denominator and has no value; section "The sliding window") and
+// the partial RoPE of "What replaced MLA" (the queries' trailing 64 channels rotated
+// in shared memory before the first S^T MMA; the output's rotated back with the
+// negated angle before it is rounded to bf16).
 #include "csa2_kernels.cuh"
 
 namespace csa2 {
@@ -194,6 +199,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     if (t == 4) {
       if (staged < 4) cp_async_wait_newest_pending();  // queries and window landed; records may still fly
       else cp_async_wait_all();
+      if (a.rope_cos != nullptr) {
+        // q = q cos + rotate_half(q) sin on channels 448 + i / 480 + i (angle i), in place
+        __syncthreads();  // every thread's query pieces have landed
+        for (int p = tid; p < kHH * 32; p += kAttnThreads) {
+          const uint32_t h = static_cast<uint32_t>(p) >> 5, i = static_cast<uint32_t>(p) & 31u;
+          const float c = __ldg(a.rope_cos + qi * 32 + i), sn = __ldg(a.rope_sin + qi * 32 + i);
+          __nv_bfloat16* pa = reinterpret_cast<__nv_bfloat16*>(Qs + tile_off(h, 448u + i));
+          __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(Qs + tile_off(h, 480u + i));
+          const float x = __bfloat162float(*pa), y = __bfloat162float(*pb);
+          *pa = __float2bfloat16_rn(x * c - y * sn);
+          *pb = __float2bfloat16_rn(y * c + x * sn);
+        }
+      }
     } else {
       cp_async_wait_all();
       __syncthreads();  // every thread's pieces of the staged records are visible
@@ -361,14 +379,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     __syncthreads();
     if (tid < kHH) {
       const float l = lred[tid] + lred[kHH + tid] + lred[2 * kHH + tid] + lred[3 * kHH + tid];
-      if (a.lse)
-        a.lse[qi * kHeads + h0 + tid] = (l > 0.0f) ? (ref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
-      alpha[tid] = l > 0.0f ? 1.0f / l : 0.0f;  // reuse: 1 / row sum
+      float lse2 = -INFINITY, inv = 0.0f;  // log2 sum-exp; O = O^T * inv
+      if (a.sinks == nullptr) {
+        if (l > 0.0f) {
+          lse2 = ref[tid] + log2f(l);
+          inv = 1.0f / l;
+        }
+      } else {
+        // the sink joins the denominator: O = O^T / (l + 2^(sink - ref)), taken relative
+        // to the larger of the two maxima so that nothing overflows
+        const float sk = __ldg(a.sinks + h0 + tid) * 1.4426950408889634f;
+        if (l > 0.0f || sk != -INFINITY) {
+          const float m2 = l > 0.0f ? fmaxf(ref[tid], sk) : sk;
+          const float lt = (l > 0.0f ? l * exp2f(ref[tid] - m2) : 0.0f) + exp2f(sk - m2);
+          lse2 = m2 + log2f(lt);
+          inv = l > 0.0f ? exp2f(ref[tid] - m2) / lt : 0.0f;
+        }
+      }
+      if (a.lse) a.lse[qi * kHeads + h0 + tid] = lse2 * 0.6931471805599453f;
+      alpha[tid] = inv;  // reuse: the output scale per head
     }
     __syncthreads();
     // O^T (TMEM lane = channel, column = head) -> bf16 [32][512] staged in the free key
     // tile, then written out with 16-byte coalesced stores
     __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(Kt);
+    float* otail = reinterpret_cast<float*>(Ps);  // [32 heads][64] fp32 rotated channels (RoPE)
+    const bool rope = a.rope_cos != nullptr;
     for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
       const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
       uint32_t r[32];
@@ -376,10 +412,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         tmem_ld32(tmem + lane_base + kOCols + static_cast<uint32_t>(c * kHH), r);
         tmem_ld_wait();
       }
+      if (rope && d >= 448u) {  // rotated back below, in fp32
+#pragma unroll
+        for (int i = 0; i < 32; ++i) otail[i * 64 + (d - 448u)] = o_started ? __uint_as_float(r[i]) * alpha[i] : 0.0f;
+        continue;
+      }
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float o = o_started ? __uint_as_float(r[i]) * alpha[i] : 0.0f;
         ostage[i * CSA2_D + d] = __float2bfloat16_rn(o);
+      }
+    }
+    if (rope) {
+      // o = o cos - rotate_half(o) sin: the rotation the values carried, undone at the
+      // query's position
+      __syncthreads();
+      for (int p = tid; p < kHH * 32; p += kAttnThreads) {
+        const int h = p >> 5, i = p & 31;
+        const float c = __ldg(a.rope_cos + qi * 32 + i), sn = __ldg(a.rope_sin + qi * 32 + i);
+        const float x = otail[h * 64 + i], y = otail[h * 64 + 32 + i];
+        ostage[h * CSA2_D + 448 + i] = __float2bfloat16_rn(x * c + y * sn);
+        ostage[h * CSA2_D + 480 + i] = __float2bfloat16_rn(y * c - x * sn);
       }
     }
     __syncthreads();

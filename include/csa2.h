@@ -115,7 +115,8 @@ typedef struct csa2_step {
   int32_t group;             /* indexer query group: 1, or 2 when consecutive queries
                                 share one request (chunked prefill)                    */
   int64_t t_max;             /* host-known upper bound of n_visible[] (grid sizing)    */
-  const void* q;             /* bf16 [n_q][heads][512], post-RoPE attention queries    */
+  const void* q;             /* bf16 [n_q][heads][512] attention queries: post-RoPE, or
+                                pre-RoPE when rope_cos / rope_sin are given           */
   const void* q_idx;         /* bf16 [n_q][heads_I][128] indexer queries (Full/Reindex)*/
   const float* w;            /* fp32 [n_q][heads_I] indexer head weights               */
   const int32_t* req;        /* [n_q] request of each query                            */
@@ -137,6 +138,17 @@ typedef struct csa2_step {
   float softmax_scale;       /* <= 0 selects 512^-0.5                                  */
   void* out;                 /* bf16 [n_q][heads][512] attention output                */
   float* lse;                /* optional fp32 [n_q][heads] natural-log sum-exp         */
+  /* Attention sinks [P2 "From MLA to DSA to HCA/CSA", "The sliding window"]: one logit
+   * per head joins every score row of the softmax and has no value vector, so the
+   * weights of the real keys sum to 1 - p_sink; lse includes it. */
+  const float* sinks;        /* optional fp32 [heads] natural-log sink logits; NULL = none */
+  /* Partial RoPE [P2 "What replaced MLA"]: the trailing 64 channels of q are rotated at
+   * the query's position, q = q cos + rotate_half(q) sin with rotate_half pairing
+   * channel 448 + i with 480 + i (angle i < 32), and the output is rotated back with the
+   * negated angle.  Cached entries are rotated before they are packed, as before. */
+  const float* rope_cos;     /* optional fp32 [n_q][32] cos of the query position's angles;
+                                NULL (with rope_sin) = q post-RoPE, O returned as is    */
+  const float* rope_sin;     /* optional fp32 [n_q][32] sin of the same angles           */
 } csa2_step;
 
 /* Message describing the last failed call on this host thread ("" if none). */

@@ -91,8 +91,11 @@ def _declare(L):
     L.or_attention.argtypes = [_u16p, ctypes.c_int32, _i32p, ctypes.c_int32, _u8p, _i32p,
                                ctypes.c_int32, ctypes.c_int32, _u16p, ctypes.c_int32,
                                ctypes.c_double, _f64p, _f64p]
+    L.or_attention_ext.argtypes = [_u16p, ctypes.c_int32, _i32p, ctypes.c_int32, _u8p, _i32p,
+                                   ctypes.c_int32, ctypes.c_int32, _u16p, ctypes.c_int32,
+                                   ctypes.c_double, _f64p, _f64p, _f64p, _f64p, _f64p]
     for f in ("or_quant_block16", "or_quant_vector", "or_pack_kv", "or_read_main", "or_read_idx",
-              "or_index_score", "or_topk", "or_attention"):
+              "or_index_score", "or_topk", "or_attention", "or_attention_ext"):
         getattr(L, f).restype = None
 
 
@@ -250,4 +253,42 @@ def attention(q_bf16, idx, kv_pages, r, win_bf16, win_len, scale=None, block_tab
     lib().or_attention(_p(q, _u16p), heads, _p(ix, _i32p), ix.size, _p(kv_pages, _u8p), btp,
                        int(max_pages), int(r), _p(win, _u16p), int(win_len), float(scale),
                        _p(O, _f64p), _p(lse, _f64p))
+    return O, lse
+
+
+# ------------------------------------------- sinks and partial RoPE [P2]
+
+def attention_ext(q_bf16, idx, kv_pages, r, win_bf16, win_len, scale=None, sinks=None, rope_cos=None,
+                  rope_sin=None, block_table=None, max_pages=0):
+    """attention() with per-head sinks and the partial RoPE of the query and output, fp64.
+
+    [P2 "From MLA to DSA to HCA/CSA", "What replaced MLA": the trailing 64 channels of q
+    are rotated at the query position (rotate_half pairs channel 448 + i with 480 + i)
+    and the output is rotated back with -sin; "The sliding window": one sink logit per
+    head joins the softmax and has no value vector.]  sinks: [H] natural-log logits;
+    rope_cos / rope_sin: [32] angles of the query position.  Returns (O [H][512], lse [H]).
+    """
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    heads = q.shape[0]
+    assert q.shape == (heads, D)
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    win = np.ascontiguousarray(win_bf16, dtype=np.uint16).reshape(-1, D)
+    assert win.shape[0] >= win_len
+    if scale is None:
+        scale = D ** -0.5
+    O = np.zeros((heads, D), np.float64)
+    lse = np.zeros(heads, np.float64)
+    bt, btp = _bt(block_table)
+    sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float64)
+    assert (rope_cos is None) == (rope_sin is None)
+    c = None if rope_cos is None else np.ascontiguousarray(rope_cos, dtype=np.float64)
+    s = None if rope_sin is None else np.ascontiguousarray(rope_sin, dtype=np.float64)
+    if sk is not None:
+        assert sk.shape == (heads,)
+    if c is not None:
+        assert c.shape == (32,) and s.shape == (32,)
+    lib().or_attention_ext(_p(q, _u16p), heads, _p(ix, _i32p), ix.size, _p(kv_pages, _u8p), btp,
+                           int(max_pages), int(r), _p(win, _u16p), int(win_len), float(scale),
+                           None if sk is None else _p(sk, _f64p), None if c is None else _p(c, _f64p),
+                           None if s is None else _p(s, _f64p), _p(O, _f64p), _p(lse, _f64p))
     return O, lse

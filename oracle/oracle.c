@@ -347,3 +347,65 @@ void or_attention(const uint16_t* q, int32_t heads, const int32_t* idx, int32_t 
   free(S);
   free(keys);
 }
+
+/* ------------------------------------------------ sinks and partial RoPE [P2]
+ * "From MLA to DSA to HCA/CSA", section "What replaced MLA" (partial RoPE and its
+ * inverse on the output): the trailing 64 channels of the query are rotated at the
+ * query's position, q = q cos + rotate_half(q) sin, and the output is rotated back
+ * with the negated angle, o = o cos - rotate_half(o) sin, where rotate_half pairs
+ * channel 448 + i with 480 + i: rotate_half(x)[448 + i] = -x[480 + i] and
+ * rotate_half(x)[480 + i] = x[448 + i] (i < 32, both halves share angle i).  The
+ * cached entries are rotated before they are packed, so keys are used as given.
+ * Section "The sliding window" (attention sinks): one logit per head is appended to
+ * each score row before the softmax and dropped after it; it has no value vector, so
+ * the weights of the real keys sum to 1 - p_sink.
+ * sinks: natural-log logits [heads] or NULL; cos/sin: [32] or NULL (no rotation).
+ * With no keys: O = 0 and lse = the sink (or -inf without sinks). */
+static void or_rotate_tail(double* x, const double* cos_, const double* sin_, double sign) {
+  for (int i = 0; i < 32; ++i) {
+    const double a = x[OR_D - 64 + i], b = x[OR_D - 32 + i];
+    x[OR_D - 64 + i] = a * cos_[i] - sign * b * sin_[i];
+    x[OR_D - 32 + i] = b * cos_[i] + sign * a * sin_[i];
+  }
+}
+
+void or_attention_ext(const uint16_t* q, int32_t heads, const int32_t* idx, int32_t k,
+                      const uint8_t* kv_pages, const int32_t* bt, int32_t max_pages, int32_t r,
+                      const uint16_t* win, int32_t win_len, double scale, const double* sinks,
+                      const double* cos_, const double* sin_, double* O, double* lse) {
+  int32_t nk = 0;
+  for (int i = 0; i < k; ++i) nk += idx[i] >= 0;
+  nk += win_len;
+  double* keys = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1) * OR_D);
+  int32_t t = 0;
+  for (int i = 0; i < k; ++i)
+    if (idx[i] >= 0) or_read_main(kv_pages, bt, max_pages, r, idx[i], keys + (int64_t)(t++) * OR_D);
+  for (int i = 0; i < win_len; ++i, ++t)
+    for (int c = 0; c < OR_D; ++c) keys[(int64_t)t * OR_D + c] = bf16_to_float(win[(int64_t)i * OR_D + c]);
+  double* S = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1));
+  double qd[OR_D];
+  for (int h = 0; h < heads; ++h) {
+    for (int c = 0; c < OR_D; ++c) qd[c] = bf16_to_float(q[(int64_t)h * OR_D + c]);
+    if (cos_) or_rotate_tail(qd, cos_, sin_, 1.0);
+    double* o = O + (int64_t)h * OR_D;
+    for (int c = 0; c < OR_D; ++c) o[c] = 0.0;
+    double mx = sinks ? sinks[h] : -INFINITY;
+    for (int j = 0; j < nk; ++j) {
+      double dot = 0.0;
+      for (int c = 0; c < OR_D; ++c) dot += qd[c] * keys[(int64_t)j * OR_D + c];
+      S[j] = scale * dot;
+      if (S[j] > mx) mx = S[j];
+    }
+    if (mx == -INFINITY) { lse[h] = -INFINITY; continue; }  /* no key and no sink */
+    double sum = sinks ? exp(sinks[h] - mx) : 0.0;
+    for (int j = 0; j < nk; ++j) { S[j] = exp(S[j] - mx); sum += S[j]; }
+    for (int j = 0; j < nk; ++j) {
+      double p = S[j] / sum;
+      for (int c = 0; c < OR_D; ++c) o[c] += p * keys[(int64_t)j * OR_D + c];
+    }
+    if (cos_) or_rotate_tail(o, cos_, sin_, -1.0);
+    lse[h] = mx + log(sum);
+  }
+  free(S);
+  free(keys);
+}

@@ -13,7 +13,8 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-2
 
 
-def _reuse(orc, csa2, n_entries, idx, req_q, win_len, seed, qscale=1.0, win_rows=None):
+def _reuse(orc, csa2, n_entries, idx, req_q, win_len, seed, qscale=1.0, win_rows=None, sinks=None, rope=None,
+           win_start=None):
     n_req = len(n_entries)
     max_pages = (max(n_entries) + 127) // 128
     cache = Cache(n_req, max_pages)
@@ -24,15 +25,23 @@ def _reuse(orc, csa2, n_entries, idx, req_q, win_len, seed, qscale=1.0, win_rows
     q = synth.normal_bf16(seed + 3, (n_q, 64, 512), scale=qscale)
     nwin = win_rows or 128 * n_q
     window = synth.normal_bf16(seed + 4, (nwin, 512))
-    win_start = np.array([128 * i if win_rows is None else i for i in range(n_q)], np.int64)
+    if win_start is None:
+        win_start = [128 * i if win_rows is None else i for i in range(n_q)]
+    win_start = np.array(win_start, np.int64)
     win_len = np.array(win_len, np.int32)
     nvis = np.array([n_entries[r] for r in req_q], np.int32)
     out = torch.zeros((n_q, 64, 512), dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros((n_q, 64), dtype=torch.float32, device="cuda")
     topk_idx = dev(np.ascontiguousarray(idx, np.int32))
+    extra = {}
+    if sinks is not None:
+        extra["sinks"] = dev(np.ascontiguousarray(sinks, np.float32))
+    if rope is not None:
+        extra["rope_cos"] = dev(np.ascontiguousarray(np.cos(rope), np.float32))
+        extra["rope_sin"] = dev(np.ascontiguousarray(np.sin(rope), np.float32))
     step = csa2.make_step(n_q=n_q, t_max=int(max(n_entries)), q=dev_bf16(q), req=dev(np.array(req_q, np.int32)),
                           n_visible=dev(nvis), window=dev_bf16(window), win_start=dev(win_start),
-                          win_len=dev(win_len), cache=cache.c, topk_idx=topk_idx, out=out, lse=lse)
+                          win_len=dev(win_len), cache=cache.c, topk_idx=topk_idx, out=out, lse=lse, **extra)
     ws = csa2.alloc_workspace(n_q, 64, int(max(n_entries)), False)
     csa2.sparse_attn_reuse(step, ws)
     assert csa2.check(ws) == (csa2.OK, 0)
@@ -40,8 +49,17 @@ def _reuse(orc, csa2, n_entries, idx, req_q, win_len, seed, qscale=1.0, win_rows
     L = lse.cpu().numpy()
     for i in range(n_q):
         ws_ = int(win_start[i])
-        Oref, lref = orc.attention(q[i], idx[i], kv_h, int(req_q[i]), window[ws_:ws_ + max(1, win_len[i])],
-                                   int(win_len[i]), None, None, max_pages)
+        if sinks is None and rope is None:
+            Oref, lref = orc.attention(q[i], idx[i], kv_h, int(req_q[i]), window[ws_:ws_ + max(1, win_len[i])],
+                                       int(win_len[i]), None, None, max_pages)
+        else:
+            # the oracle takes the angles the kernel saw (fp32), in fp64
+            rc = None if rope is None else np.cos(rope[i]).astype(np.float32)
+            rs = None if rope is None else np.sin(rope[i]).astype(np.float32)
+            Oref, lref = orc.attention_ext(q[i], idx[i], kv_h, int(req_q[i]),
+                                           window[ws_:ws_ + max(1, win_len[i])], int(win_len[i]), None,
+                                           None if sinks is None else np.asarray(sinks, np.float32),
+                                           rc, rs, None, max_pages)
         err = np.abs(O[i] - Oref).max()
         assert err <= TOL, (i, err)
         fin = np.isfinite(lref)
@@ -81,3 +99,38 @@ def test_attn_shared_window_rows_prefill_style(orc, csa2):
     n_q = 3
     idx = np.stack([synth.distinct_indices(10 + i, 1200, 512) for i in range(n_q)])
     _reuse(orc, csa2, n, idx, [0] * n_q, [128, 128, 128], seed=53, win_rows=130)
+
+
+def test_attn_sinks_and_partial_rope(orc, csa2):
+    """Per-head sinks join the softmax; the query's trailing 64 channels are rotated at
+    its position and the output rotated back ("From MLA to DSA to HCA/CSA", "The sliding
+    window" and "What replaced MLA")."""
+    n = [1800]
+    n_q = 3
+    idx = np.stack([synth.distinct_indices(20 + i, 1800, 512) for i in range(n_q)])
+    sinks = 2.0 * synth.normal_f32(21, (64,))
+    sinks[:4] = [-30.0, 0.0, 8.0, 30.0]  # negligible, even, dominant, overwhelming
+    rope = synth.rng(22).uniform(-np.pi, np.pi, (n_q, 32))
+    _reuse(orc, csa2, n, idx, [0] * n_q, [128, 77, 0], seed=54, qscale=2.0, sinks=sinks, rope=rope)
+
+
+def test_attn_rope_only_and_sinks_only(orc, csa2):
+    n = [900]
+    idx = np.stack([synth.distinct_indices(23, 900, 512), synth.distinct_indices(24, 900, 512)])
+    rope = synth.rng(25).uniform(-np.pi, np.pi, (2, 32))
+    _reuse(orc, csa2, n, idx, [0, 0], [128, 128], seed=55, qscale=4.0, rope=rope)
+    _reuse(orc, csa2, n, idx, [0, 0], [128, 3], seed=56, sinks=synth.normal_f32(26, (64,)))
+
+
+def test_attn_bounded_replay_window(orc, csa2):
+    """SWA bounded replay ("DeepSeek-V4.1", bounded replay): a replay from position s
+    lets the query at i see the local keys [max(s, i - 127), i]; the window rows of a
+    chunk are one buffer and each query's start and length follow that rule."""
+    n = [1000]
+    s0, base = 40, 0                          # replay starts at position 40 of the window buffer
+    pos = [40, 41, 100, 167, 168, 300]        # query positions (buffer rows)
+    starts = [max(s0, i - 127) for i in pos]
+    lens = [i - st + 1 for i, st in zip(pos, starts)]
+    assert lens == [1, 2, 61, 128, 128, 128]
+    idx = np.stack([synth.distinct_indices(30 + i, 1000, 512) for i in range(len(pos))])
+    _reuse(orc, csa2, n, idx, [0] * len(pos), lens, seed=57, win_rows=301 + base, win_start=starts)
