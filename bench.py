@@ -317,7 +317,7 @@ def _timed(csa2, fn, warmup, steps):
     return ms, kernels
 
 
-def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3):
+def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3, sinks_rope=False):
     import synth
     mp = (T + 127) // 128
     cache = _device_cache(csa2, dev, B, T - 1, mp, seed, frac)
@@ -329,6 +329,12 @@ def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3):
     new_key = synth.torch_normal_bf16(sb + 5, (B, DI), dev)
     window = synth.torch_normal_bf16(sb + 6, (B * WIN, D), dev)
     out = torch.empty((B, HEADS, D), dtype=torch.bfloat16, device=dev)
+    extra = {}
+    if sinks_rope:  # per-head sinks and the partial RoPE of q and O, angles of position T - 1
+        ang = (T - 1) * torch.pow(10000.0, -torch.arange(32, dtype=torch.float64, device=dev) / 32.0)
+        extra = {"sinks": synth.torch_normal_f32(sb + 7, (HEADS,), dev),
+                 "rope_cos": torch.cos(ang).float().expand(B, 32).contiguous(),
+                 "rope_sin": torch.sin(ang).float().expand(B, 32).contiguous()}
     step = csa2.make_step(n_q=B, t_max=T, q=q, req=torch.arange(B, dtype=torch.int32, device=dev),
                           n_visible=torch.full((B,), T, dtype=torch.int32, device=dev), window=window,
                           win_start=torch.arange(B, dtype=torch.int64, device=dev) * WIN,
@@ -337,7 +343,7 @@ def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3):
                           lse=torch.empty((B, HEADS), dtype=torch.float32, device=dev), q_idx=q_idx, w=w,
                           heads_I=HEADS_I, group=1, n_new=B, new_latent=new_lat, new_idx_key=new_key,
                           new_req=torch.arange(B, dtype=torch.int32, device=dev),
-                          new_pos=torch.full((B,), T - 1, dtype=torch.int64, device=dev))
+                          new_pos=torch.full((B,), T - 1, dtype=torch.int64, device=dev), **extra)
     ws = csa2.alloc_workspace(B, HEADS_I, T, True, dev)
     ms, kernels = _timed(csa2, lambda: csa2.sparse_attn_full(step, ws), warmup, steps)
     st, info = csa2.check(ws)
@@ -350,8 +356,9 @@ def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3):
 
 def measure_extra(dev, hbm_peak, bf16_tflops):
     """The other workloads of the layer, each in its own line: the tiny decode, Reuse and
-    Reindex at 128 x 262,144, the million-token decode with its ratio-2 layer (1 % of
-    entries x 8), and a 4,096-token chunked prefill on 262,144 cached entries."""
+    Reindex at 128 x 262,144, the headline decode with sinks and fused partial RoPE, the
+    million-token decode with its ratio-2 layer (1 % of entries x 8), and a 4,096-token
+    chunked prefill on 262,144 cached entries."""
     import synth
     from fp4_compressed_sparse_csa2_gb300 import csa2
     lines = []
@@ -400,6 +407,8 @@ def measure_extra(dev, hbm_peak, bf16_tflops):
                 "device_status": st}
 
     attempt(reuse_reindex)
+    attempt(lambda: dict(_decode_line(csa2, dev, "Full decode with per-head sinks and fused partial RoPE, B=64, "
+                                      "T=131072", 64, 131072, 3200, sinks_rope=True), note="next row N4"))
     attempt(lambda: dict(_decode_line(csa2, dev, "million-token Full decode, B=8, T=1048576, 1% of entries x8", 8,
                                       1 << 20, 3000, 0.01), note="decoder layer"))
     attempt(lambda: dict(_decode_line(csa2, dev, "ratio-2 layer Full decode, B=8, 524288 pooled entries, 1% x8", 8,

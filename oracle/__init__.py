@@ -94,8 +94,16 @@ def _declare(L):
     L.or_attention_ext.argtypes = [_u16p, ctypes.c_int32, _i32p, ctypes.c_int32, _u8p, _i32p,
                                    ctypes.c_int32, ctypes.c_int32, _u16p, ctypes.c_int32,
                                    ctypes.c_double, _f64p, _f64p, _f64p, _f64p, _f64p]
+    L.or_e8m0_exponent.argtypes = [ctypes.c_double]
+    L.or_e8m0_exponent.restype = ctypes.c_int32
+    L.or_pack_window.argtypes = [_u16p, _i32p, _i64p, ctypes.c_int64, _u8p]
+    L.or_read_window.argtypes = [_u8p, ctypes.c_int32, ctypes.c_int64, _f64p]
+    L.or_attention_ring.argtypes = [_u16p, ctypes.c_int32, _i32p, ctypes.c_int32, _u8p, _i32p,
+                                    ctypes.c_int32, ctypes.c_int32, _u8p, ctypes.c_int64, ctypes.c_int32,
+                                    ctypes.c_double, _f64p, _f64p, _f64p, _f64p, _f64p]
     for f in ("or_quant_block16", "or_quant_vector", "or_pack_kv", "or_read_main", "or_read_idx",
-              "or_index_score", "or_topk", "or_attention", "or_attention_ext"):
+              "or_index_score", "or_topk", "or_attention", "or_attention_ext", "or_pack_window",
+              "or_read_window", "or_attention_ring"):
         getattr(L, f).restype = None
 
 
@@ -291,4 +299,62 @@ def attention_ext(q_bf16, idx, kv_pages, r, win_bf16, win_len, scale=None, sinks
                            int(max_pages), int(r), _p(win, _u16p), int(win_len), float(scale),
                            None if sk is None else _p(sk, _f64p), None if c is None else _p(c, _f64p),
                            None if s is None else _p(s, _f64p), _p(O, _f64p), _p(lse, _f64p))
+    return O, lse
+
+
+# ------------------------------------------------------------- FP8 window ring [P1]
+WIN, WIN_BYTES = 128, 528
+
+
+def e8m0_exponent(amax: float) -> int:
+    """The window block's scale exponent: the smallest e with amax <= 448 * 2^e, clamped
+    to [-127, 127] (an all-zero block: -127)."""
+    return int(lib().or_e8m0_exponent(float(amax)))
+
+
+def alloc_ring(n_req: int) -> np.ndarray:
+    """A window ring of W = 128 slots of 528 bytes per request."""
+    return np.zeros(n_req * WIN * WIN_BYTES, np.uint8)
+
+
+def pack_window(rows_bf16, req, pos, ring):
+    """Pack bf16 window rows into slot pos mod 128 of each request's ring.
+
+    [P1 "Four bits for the main KV, eight for the window": 512 E4M3 bytes plus 16 E8M0
+    scales, 528 bytes; "Definition and the bounded cache": position i in slot i mod W.]
+    """
+    rows = np.ascontiguousarray(rows_bf16, dtype=np.uint16).reshape(-1, D)
+    req = np.ascontiguousarray(req, dtype=np.int32)
+    pos = np.ascontiguousarray(pos, dtype=np.int64)
+    assert rows.shape[0] == req.size == pos.size
+    lib().or_pack_window(_p(rows, _u16p), _p(req, _i32p), _p(pos, _i64p), rows.shape[0], _p(ring, _u8p))
+
+
+def read_window(ring, r: int, p: int) -> np.ndarray:
+    """Dequantised window entry of position p of request r (fp64, exact)."""
+    out = np.zeros(D, np.float64)
+    lib().or_read_window(_p(ring, _u8p), int(r), int(p), _p(out, _f64p))
+    return out
+
+
+def attention_ring(q_bf16, idx, kv_pages, r, ring, win_pos, win_len, scale=None, sinks=None, rope_cos=None,
+                   rope_sin=None, block_table=None, max_pages=0):
+    """attention_ext() with the window keys taken from the FP8 ring: the entries of
+    positions win_pos - win_len + 1 .. win_pos of request r.  Returns (O [H][512], lse [H])."""
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    heads = q.shape[0]
+    assert q.shape == (heads, D)
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    if scale is None:
+        scale = D ** -0.5
+    O = np.zeros((heads, D), np.float64)
+    lse = np.zeros(heads, np.float64)
+    bt, btp = _bt(block_table)
+    sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float64)
+    c = None if rope_cos is None else np.ascontiguousarray(rope_cos, dtype=np.float64)
+    s = None if rope_sin is None else np.ascontiguousarray(rope_sin, dtype=np.float64)
+    lib().or_attention_ring(_p(q, _u16p), heads, _p(ix, _i32p), ix.size, _p(kv_pages, _u8p), btp,
+                            int(max_pages), int(r), _p(ring, _u8p), int(win_pos), int(win_len), float(scale),
+                            None if sk is None else _p(sk, _f64p), None if c is None else _p(c, _f64p),
+                            None if s is None else _p(s, _f64p), _p(O, _f64p), _p(lse, _f64p))
     return O, lse

@@ -369,19 +369,10 @@ static void or_rotate_tail(double* x, const double* cos_, const double* sin_, do
   }
 }
 
-void or_attention_ext(const uint16_t* q, int32_t heads, const int32_t* idx, int32_t k,
-                      const uint8_t* kv_pages, const int32_t* bt, int32_t max_pages, int32_t r,
-                      const uint16_t* win, int32_t win_len, double scale, const double* sinks,
-                      const double* cos_, const double* sin_, double* O, double* lse) {
-  int32_t nk = 0;
-  for (int i = 0; i < k; ++i) nk += idx[i] >= 0;
-  nk += win_len;
-  double* keys = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1) * OR_D);
-  int32_t t = 0;
-  for (int i = 0; i < k; ++i)
-    if (idx[i] >= 0) or_read_main(kv_pages, bt, max_pages, r, idx[i], keys + (int64_t)(t++) * OR_D);
-  for (int i = 0; i < win_len; ++i, ++t)
-    for (int c = 0; c < OR_D; ++c) keys[(int64_t)t * OR_D + c] = bf16_to_float(win[(int64_t)i * OR_D + c]);
+/* S, softmax (with the sink) and the output over nk fp64 keys; q rotated first and the
+ * output rotated back when cos_ is given. */
+static void or_attend(const uint16_t* q, int32_t heads, const double* keys, int32_t nk, double scale,
+                      const double* sinks, const double* cos_, const double* sin_, double* O, double* lse) {
   double* S = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1));
   double qd[OR_D];
   for (int h = 0; h < heads; ++h) {
@@ -407,5 +398,86 @@ void or_attention_ext(const uint16_t* q, int32_t heads, const int32_t* idx, int3
     lse[h] = mx + log(sum);
   }
   free(S);
+}
+
+void or_attention_ext(const uint16_t* q, int32_t heads, const int32_t* idx, int32_t k,
+                      const uint8_t* kv_pages, const int32_t* bt, int32_t max_pages, int32_t r,
+                      const uint16_t* win, int32_t win_len, double scale, const double* sinks,
+                      const double* cos_, const double* sin_, double* O, double* lse) {
+  int32_t nk = 0;
+  for (int i = 0; i < k; ++i) nk += idx[i] >= 0;
+  nk += win_len;
+  double* keys = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1) * OR_D);
+  int32_t t = 0;
+  for (int i = 0; i < k; ++i)
+    if (idx[i] >= 0) or_read_main(kv_pages, bt, max_pages, r, idx[i], keys + (int64_t)(t++) * OR_D);
+  for (int i = 0; i < win_len; ++i, ++t)
+    for (int c = 0; c < OR_D; ++c) keys[(int64_t)t * OR_D + c] = bf16_to_float(win[(int64_t)i * OR_D + c]);
+  or_attend(q, heads, keys, nk, scale, sinks, cos_, sin_, O, lse);
+  free(keys);
+}
+
+/* ------------------------------------------------ FP8 window ring [P1]
+ * "DeepSeek's Attention and KV Cache - From MLA to CSA2", "Four bits for the main KV,
+ * eight for the window": a window entry is 512 E4M3 bytes (RoPE channels included)
+ * plus 16 E8M0 scales, 528 bytes, one scale per 32 channels.  "Definition and the
+ * bounded cache": the entry of position i lives in slot i mod W of a W-slot ring
+ * (W = 128).  Scale (the pages are silent): the smallest power of two 2^e with
+ * amax <= 448 * 2^e, so that no element clips, e clamped to the E8M0 range [-127, 127];
+ * an all-zero block takes e = -127.  Element: E4M3 round-to-nearest-even of x / 2^e
+ * (an exact division).  Record: bytes [0, 512) the codes in channel order, then the
+ * 16 E8M0 codes e + 127 in block order. */
+#define OR_WIN 128
+#define OR_WIN_BYTES 528
+
+int32_t or_e8m0_exponent(double amax) {
+  if (!(amax > 0.0)) return -127;
+  int E;
+  frexp(amax, &E); /* amax in [2^(E-1), 2^E); 448 * 2^(E-10) < 2^(E-1) <= amax < 448 * 2^(E-8) */
+  int e = amax <= ldexp(448.0, E - 9) ? E - 9 : E - 8;
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
+void or_pack_window(const uint16_t* rows, const int32_t* req, const int64_t* pos, int64_t n, uint8_t* ring) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint8_t* rec = ring + ((int64_t)req[i] * OR_WIN + pos[i] % OR_WIN) * OR_WIN_BYTES;
+    for (int b = 0; b < OR_D / 32; ++b) {
+      double amax = 0.0;
+      for (int c = 0; c < 32; ++c) {
+        double v = fabs((double)bf16_to_float(rows[i * OR_D + 32 * b + c]));
+        if (v > amax) amax = v;
+      }
+      int e = or_e8m0_exponent(amax);
+      for (int c = 0; c < 32; ++c) {
+        double x = (double)bf16_to_float(rows[i * OR_D + 32 * b + c]);
+        rec[32 * b + c] = or_e4m3_encode((float)ldexp(x, -e)); /* exact: |x / 2^e| <= 448 */
+      }
+      rec[OR_D + b] = (uint8_t)(e + 127);
+    }
+  }
+}
+
+void or_read_window(const uint8_t* ring, int32_t r, int64_t p, double* out) {
+  const uint8_t* rec = ring + ((int64_t)r * OR_WIN + p % OR_WIN) * OR_WIN_BYTES;
+  for (int c = 0; c < OR_D; ++c) out[c] = or_e4m3_decode(rec[c]) * ldexp(1.0, (int)rec[OR_D + c / 32] - 127);
+}
+
+/* Attention whose window keys are the ring entries of positions win_pos - win_len + 1
+ * .. win_pos of request r (the selected entries as in or_attention_ext). */
+void or_attention_ring(const uint16_t* q, int32_t heads, const int32_t* idx, int32_t k,
+                       const uint8_t* kv_pages, const int32_t* bt, int32_t max_pages, int32_t r,
+                       const uint8_t* ring, int64_t win_pos, int32_t win_len, double scale, const double* sinks,
+                       const double* cos_, const double* sin_, double* O, double* lse) {
+  int32_t nk = 0;
+  for (int i = 0; i < k; ++i) nk += idx[i] >= 0;
+  nk += win_len;
+  double* keys = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1) * OR_D);
+  int32_t t = 0;
+  for (int i = 0; i < k; ++i)
+    if (idx[i] >= 0) or_read_main(kv_pages, bt, max_pages, r, idx[i], keys + (int64_t)(t++) * OR_D);
+  for (int i = 0; i < win_len; ++i, ++t) or_read_window(ring, r, win_pos - i, keys + (int64_t)t * OR_D);
+  or_attend(q, heads, keys, nk, scale, sinks, cos_, sin_, O, lse);
   free(keys);
 }
