@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
 # sizes fixed by the pages (mirrors the enum in include/csa2.h)
 D, DI, BLOCK = 512, 128, 16
-KV_BYTES, IDX_BYTES = 288, 72
+KV_BYTES, IDX_BYTES, WIN_BYTES = 288, 72, 528
 TOPK, WIN, HEADS, PAGE = 512, 128, 64, 128
 KV_PAGE_BYTES, IDX_PAGE_BYTES = PAGE * KV_BYTES, PAGE * IDX_BYTES
 
@@ -46,7 +46,8 @@ class csa2_step(ctypes.Structure):
                 ("new_pos", ctypes.c_void_p), ("cache", csa2_cache), ("topk_idx", ctypes.c_void_p),
                 ("scores", ctypes.c_void_p), ("ld", ctypes.c_int64), ("softmax_scale", ctypes.c_float),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("sinks", ctypes.c_void_p),
-                ("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p)]
+                ("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p), ("win_ring", ctypes.c_void_p),
+                ("win_ring_reqs", ctypes.c_int32)]
 
 
 def _load():
@@ -61,6 +62,7 @@ def _load():
     L.csa2_index_score.argtypes = [vp, vp, i32, vp, vp, i64, i32, i64, ctypes.POINTER(csa2_cache), vp, i64, vp,
                                    sz, vp]
     L.csa2_topk.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp, sz, vp]
+    L.csa2_pack_window.argtypes = [vp, vp, vp, i64, vp, i32, vp, sz, vp]
     for f in ("csa2_sparse_attn_full", "csa2_sparse_attn_reindex", "csa2_sparse_attn_reuse"):
         getattr(L, f).argtypes = [ctypes.POINTER(csa2_step), vp, sz, vp]
     L.csa2_topk_noalloc.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp]
@@ -69,7 +71,7 @@ def _load():
     L.csa2_launch_count.restype = i64
     L.csa2_trace_enable.argtypes = [i32]
     L.csa2_trace_read.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
-    for f in ("csa2_pack_kv", "csa2_index_score", "csa2_topk", "csa2_sparse_attn_full",
+    for f in ("csa2_pack_kv", "csa2_pack_window", "csa2_index_score", "csa2_topk", "csa2_sparse_attn_full",
               "csa2_sparse_attn_reindex", "csa2_sparse_attn_reuse", "csa2_check", "csa2_trace_enable",
               "csa2_trace_read"):
         getattr(L, f).restype = ctypes.c_int
@@ -117,6 +119,14 @@ def pack_kv(latent, idx_key, req, pos, cache: csa2_cache, ws, stream=None):
                             ws.numel(), _stream(stream)))
 
 
+def pack_window(rows, req, pos, ring, n_ring, ws, stream=None):
+    """FP8 window entries of bf16 rows [n][512] into slot pos % 128 of each request's ring
+    (uint8 [n_ring * 128 * 528])."""
+    n = 0 if rows is None else rows.shape[0]
+    _check(lib.csa2_pack_window(_ptr(rows), _ptr(req), _ptr(pos), n, _ptr(ring), int(n_ring), _ptr(ws), ws.numel(),
+                                _stream(stream)))
+
+
 def index_score(q_idx, w, heads_I, req, n_visible, n_q, group, t_max, cache, scores, ld, ws, stream=None):
     _check(lib.csa2_index_score(_ptr(q_idx), _ptr(w), int(heads_I), _ptr(req), _ptr(n_visible), int(n_q),
                                 int(group), int(t_max), ctypes.byref(cache), _ptr(scores), int(ld), _ptr(ws),
@@ -137,14 +147,14 @@ def topk_noalloc(scores, ld, n_visible, n_q, t_max, k, out_idx, stream=None):
 def make_step(*, n_q, t_max, q, req, n_visible, window, win_start, win_len, cache, topk_idx, out, q_idx=None,
               w=None, heads_I=64, group=1, n_new=0, new_latent=None, new_idx_key=None, new_req=None, new_pos=None,
               scores=None, ld=0, softmax_scale=0.0, lse=None, sinks=None, rope_cos=None,
-              rope_sin=None) -> csa2_step:
+              rope_sin=None, win_ring=None, win_ring_reqs=0) -> csa2_step:
     s = csa2_step(int(n_q), HEADS, int(heads_I), TOPK, int(group), int(t_max), _ptr(q), _ptr(q_idx), _ptr(w),
                   _ptr(req), _ptr(n_visible), _ptr(window), _ptr(win_start), _ptr(win_len), int(n_new),
                   _ptr(new_latent), _ptr(new_idx_key), _ptr(new_req), _ptr(new_pos), cache, _ptr(topk_idx),
                   _ptr(scores), int(ld), float(softmax_scale), _ptr(out), _ptr(lse), _ptr(sinks), _ptr(rope_cos),
-                  _ptr(rope_sin))
+                  _ptr(rope_sin), _ptr(win_ring), int(win_ring_reqs))
     s._keep = (q, req, n_visible, window, win_start, win_len, cache, topk_idx, out, q_idx, w, new_latent,
-               new_idx_key, new_req, new_pos, scores, lse, sinks, rope_cos, rope_sin)
+               new_idx_key, new_req, new_pos, scores, lse, sinks, rope_cos, rope_sin, win_ring)
     return s
 
 

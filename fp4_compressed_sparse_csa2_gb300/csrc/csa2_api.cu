@@ -247,6 +247,8 @@ csa2_status run_attn(const csa2_step& s, int32_t* err, cudaStream_t stream) {
   a.sinks = s.sinks;
   a.rope_cos = s.rope_cos;
   a.rope_sin = s.rope_sin;
+  a.win_ring = s.win_ring;
+  a.win_ring_reqs = s.win_ring_reqs;
   trace_begin(kAttn, stream);
   const cudaError_t e = launch_attn(a, stream);
   trace_end(kAttn, stream);
@@ -264,8 +266,11 @@ csa2_status check_step(const csa2_step* s, Mode mode) {
     if (!s->q || !aligned(s->q, 16)) return fail(CSA2_ERR_INVALID_ARG, "q must be a 16-byte aligned device pointer");
     if (!s->out) return fail(CSA2_ERR_INVALID_ARG, "out is NULL");
     if (!s->req || !s->n_visible) return fail(CSA2_ERR_INVALID_ARG, "req and n_visible are required");
-    if (!s->window || !aligned(s->window, 16) || !s->win_start || !s->win_len)
-      return fail(CSA2_ERR_INVALID_ARG, "window, win_start and win_len are required (window 16-byte aligned)");
+    if (!s->win_start || !s->win_len) return fail(CSA2_ERR_INVALID_ARG, "win_start and win_len are required");
+    if (s->win_ring == nullptr && (!s->window || !aligned(s->window, 16)))
+      return fail(CSA2_ERR_INVALID_ARG, "window rows (16-byte aligned) are required without a window ring");
+    if (s->win_ring != nullptr && (!aligned(s->win_ring, 16) || s->win_ring_reqs <= 0))
+      return fail(CSA2_ERR_INVALID_ARG, "win_ring must be 16-byte aligned with win_ring_reqs > 0");
     if (!s->topk_idx) return fail(CSA2_ERR_INVALID_ARG, "topk_idx is NULL");
     if ((s->rope_cos == nullptr) != (s->rope_sin == nullptr))
       return fail(CSA2_ERR_INVALID_ARG, "rope_cos and rope_sin go together");
@@ -333,6 +338,26 @@ csa2_status csa2_pack_kv(const void* latent, const void* idx_key, const int32_t*
     return fail(CSA2_ERR_INVALID_ARG, "latent/idx_key (16-byte aligned), req and pos are required");
   return run_pack(latent, idx_key, req, pos, n, *cache, nullptr, 0, 64, 1, nullptr, err_word(ws),
                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa2_status csa2_pack_window(const void* rows, const int32_t* req, const int64_t* pos, int64_t n, uint8_t* ring,
+                             int32_t n_ring, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  if (n < 0) return fail(CSA2_ERR_INVALID_ARG, "n must be >= 0");
+  csa2_status st = check_ws(ws, ws_bytes, kHeader);
+  if (st != CSA2_OK) return st;
+  if (n == 0) return CSA2_OK;
+  if (!rows || !aligned(rows, 16) || !req || !pos) return fail(CSA2_ERR_INVALID_ARG, "rows (16-byte aligned), req and pos are required");
+  if (!ring || !aligned(ring, 16) || n_ring <= 0) return fail(CSA2_ERR_INVALID_ARG, "ring must be 16-byte aligned with n_ring > 0");
+  WinPackArgs a{};
+  a.rows = static_cast<const __nv_bfloat16*>(rows);
+  a.req = req;
+  a.pos = pos;
+  a.n = n;
+  a.ring = ring;
+  a.n_ring = n_ring;
+  a.err = err_word(ws);
+  const cudaError_t e = launch_pack_window(a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "window pack kernel");
 }
 
 csa2_status csa2_index_score(const void* q_idx, const float* w, int32_t heads_I, const int32_t* req,

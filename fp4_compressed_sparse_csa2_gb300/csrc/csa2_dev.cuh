@@ -318,6 +318,24 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
   return (c & 0x80u) ? -v : v;
 }
 
+// FP8 window block scale: the smallest e with amax <= 448 * 2^e, clamped to
+// [-127, 127] (amax == 0: -127).  amax lies in [2^(E-1), 2^E), so e is E - 9 or E - 8;
+// one exact comparison decides.
+__device__ __forceinline__ int e8m0_exponent(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  int E;
+  frexpf(amax, &E);
+  const int e = amax <= ldexpf(448.0f, E - 9) ? E - 9 : E - 8;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Two E4M3 codes (low byte first) -> f16x2, exactly (hardware conversion).
+__device__ __forceinline__ __half2 e4m3x2_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(two));
+  return *reinterpret_cast<__half2*>(&r);
+}
+
 // Quantise 16 fp32 values: returns the scale code; writes 8 bytes of nibbles
 // (value 2i in the low nibble of byte i).
 __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], uint32_t& nib_lo, uint32_t& nib_hi) {

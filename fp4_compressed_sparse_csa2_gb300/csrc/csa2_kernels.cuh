@@ -80,6 +80,18 @@ struct AttnArgs {
   const float* sinks;     // [64] natural-log sink logits or nullptr
   const float* rope_cos;  // [n_q][32] or nullptr (then rope_sin too)
   const float* rope_sin;
+  const uint8_t* win_ring;  // FP8 window ring [win_ring_reqs][128][528] or nullptr
+  int32_t win_ring_reqs;
+};
+
+struct WinPackArgs {
+  const __nv_bfloat16* rows;  // [n][512]
+  const int32_t* req;
+  const int64_t* pos;
+  int64_t n;
+  uint8_t* ring;  // [n_ring][128][528]
+  int32_t n_ring;
+  int32_t* err;
 };
 
 using TraceFn = void (*)(int, cudaStream_t);
@@ -126,5 +138,6 @@ cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes);
 cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream);
 size_t attn_smem_bytes();
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_pack_window(const WinPackArgs& a, cudaStream_t stream);
 
 }  // namespace csa2

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     }
     cp_async_commit();
     const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
-    for (int c = tid; c < 128 * 64; c += kAttnThreads) {
+    for (int c = tid; a.win_ring == nullptr && c < 128 * 64; c += kAttnThreads) {  // bf16 window rows
       uint32_t r, ch;
       tile_item(static_cast<uint32_t>(c), 128, r, ch);
       const bool ok = static_cast<int32_t>(r) < wl;
@@ -210,6 +210,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
           const float x = __bfloat162float(*pa), y = __bfloat162float(*pb);
           *pa = __float2bfloat16_rn(x * c - y * sn);
           *pb = __float2bfloat16_rn(y * c + x * sn);
+        }
+      }
+      if (a.win_ring != nullptr) {
+        // FP8 window ring: row i of the tile is the entry of position newest - i, read
+        // after the wait on the previous kernel (the ring is written by an earlier call);
+        // E4M3 -> f16 in hardware, times the block's 2^e, -> bf16 (exact)
+        const int64_t newest = __ldg(a.win_start + qi);
+        const int32_t r = __ldg(a.req + qi);
+        const bool ring_ok = r >= 0 && r < a.win_ring_reqs && newest - wl + 1 >= 0;
+        if (!ring_ok && wl > 0 && tid == 0) report(a.err, CSA2_ERR_DEVICE, kInfoPos);
+#pragma unroll 2
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t task = static_cast<uint32_t>(tid + kAttnThreads * i);
+          const uint32_t row = (task & 7u) | (((task >> 5) & 15u) << 3);
+          const uint32_t j = ((task >> 3) & 3u) | ((task >> 9) << 2);
+          uint8_t* dst = Kt + tile_off(row, 32 * j);
+          if (!ring_ok || static_cast<int32_t>(row) >= wl) {  // no entry: zeros (masked)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + m * 128) = make_uint4(0, 0, 0, 0);
+            continue;
+          }
+          const int64_t pos = newest - row;
+          const uint8_t* rec = a.win_ring + (static_cast<int64_t>(r) * CSA2_WIN + pos % CSA2_WIN) * CSA2_WIN_BYTES;
+          const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(rec + 32 * j));
+          const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(rec + 32 * j + 16));
+          const float sc = ldexpf(1.0f, static_cast<int>(__ldg(rec + 512 + j)) - 127);
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = __half22float2(e4m3x2_f16x2((cw[2 * m + (k >> 1)] >> (16 * (k & 1))) & 0xFFFFu));
+              const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+              o[k] = *reinterpret_cast<const uint32_t*>(&bv);
+            }
+            *reinterpret_cast<uint4*>(dst + m * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
         }
       }
     } else {

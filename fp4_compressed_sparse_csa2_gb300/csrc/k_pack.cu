@@ -90,6 +90,52 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
   gp[idx_sf_off(nib_bytes, n, bb)] = static_cast<uint8_t>(sc);
 }
 
+// FP8 window ring ("Four bits for the main KV, eight for the window": 512 E4M3 bytes
+// plus 16 E8M0 scales per entry; "Definition and the bounded cache": position i in slot
+// i mod 128).  One thread per 32-channel block: four 16-byte loads, the block's
+// power-of-two scale, 32 E4M3 conversions of exact quotients, two 16-byte stores and a
+// scale byte.
+__global__ void __launch_bounds__(256) pack_window_kernel(WinPackArgs a) {
+  pdl_trigger();
+  pdl_wait();  // earlier kernels may still read the slots written here
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (item >= a.n * 16) return;
+  const int64_t i = item >> 4;
+  const int b = static_cast<int>(item & 15);
+  const int32_t r = a.req[i];
+  const int64_t p = a.pos[i];
+  if (r < 0 || r >= a.n_ring || p < 0) {
+    report(a.err, CSA2_ERR_DEVICE, kInfoPos);
+    return;
+  }
+  float x[32];
+  load16(a.rows + i * kD + 32 * b, *reinterpret_cast<float(*)[16]>(&x[0]));
+  load16(a.rows + i * kD + 32 * b + 16, *reinterpret_cast<float(*)[16]>(&x[16]));
+  float amax = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) amax = fmaxf(amax, fabsf(x[c]));
+  const int e = e8m0_exponent(amax);
+  uint32_t w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) v |= cvt_e4m3(ldexpf(x[4 * k + m], -e)) << (8 * m);  // exact quotient
+    w[k] = v;
+  }
+  uint8_t* rec = a.ring + (static_cast<int64_t>(r) * CSA2_WIN + p % CSA2_WIN) * CSA2_WIN_BYTES;
+  uint4* dst = reinterpret_cast<uint4*>(rec + 32 * b);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  rec[512 + b] = static_cast<uint8_t>(e + 127);
+}
+
+cudaError_t launch_pack_window(const WinPackArgs& a, cudaStream_t stream) {
+  if (a.n == 0) return cudaSuccess;
+  const int64_t blocks = (a.n * 16 + 255) / 256;
+  return launch_pdl(pack_window_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, nullptr, a);
+}
+
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t stream) {
   const int64_t items = a.n_new * 40 + a.n_groups * 128 * 8;
   if (items == 0) return cudaSuccess;

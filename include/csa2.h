@@ -61,6 +61,8 @@ typedef enum csa2_status {
  *   CSA2_TOPK   selected entries per query, 512 [P1 "DeepSeek-V4.1"; P3 section 2]
  *   CSA2_WIN    sliding-window entries, 128 [P1 "DeepSeek-V4"; P4 "Two branches"]
  *   CSA2_HEADS  attention query heads sharing one KV entry, 64 [P2 "Part 2"; P4]
+ *   CSA2_WIN_BYTES FP8 window entry: 512 E4M3 bytes + 16 E8M0 scales = 528 [P1 "Four
+ *               bits for the main KV, eight for the window"]
  * Layout choice of this library (the pages give entry sizes only):
  *   CSA2_PAGE   entries per cache page, 128. */
 enum {
@@ -74,7 +76,8 @@ enum {
   CSA2_HEADS = 64,
   CSA2_PAGE = 128,
   CSA2_KV_PAGE_BYTES = 36864,  /* 128 x 288 */
-  CSA2_IDX_PAGE_BYTES = 9216   /* 128 x 72  */
+  CSA2_IDX_PAGE_BYTES = 9216,  /* 128 x 72  */
+  CSA2_WIN_BYTES = 528
 };
 
 /* The global cache of one CSA2 Full layer: a paged main-KV cache and a paged
@@ -149,6 +152,12 @@ typedef struct csa2_step {
   const float* rope_cos;     /* optional fp32 [n_q][32] cos of the query position's angles;
                                 NULL (with rope_sin) = q post-RoPE, O returned as is    */
   const float* rope_sin;     /* optional fp32 [n_q][32] sin of the same angles           */
+  /* FP8 window ring (see csa2_pack_window).  When win_ring is set, the window of query
+   * q is the ring entries of positions win_start[q] - win_len[q] + 1 .. win_start[q] of
+   * request req[q] (win_start is then the newest window position) and `window` is not
+   * read; NULL = bf16 window rows as above. */
+  const uint8_t* win_ring;   /* optional [win_ring_reqs][128][528]                      */
+  int32_t win_ring_reqs;     /* requests in win_ring (bounds check)                    */
 } csa2_step;
 
 /* Message describing the last failed call on this host thread ("" if none). */
@@ -167,6 +176,19 @@ size_t csa2_workspace_bytes(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t
 csa2_status csa2_pack_kv(const void* latent, const void* idx_key, const int32_t* req,
                          const int64_t* pos, int64_t n, const csa2_cache* cache, void* ws,
                          size_t ws_bytes, csa2_stream_t stream);
+
+/* FP8 window ring [P1 "Four bits for the main KV, eight for the window": a window
+ * entry is 512 E4M3 bytes plus 16 E8M0 scales, 528 bytes; P1 "Definition and the
+ * bounded cache": position i lives in slot i mod 128 of its request's ring].
+ * ring: [n_ring][128][528] bytes, 16-byte aligned; entry layout: bytes [0, 512) the
+ * E4M3 codes in channel order, [512, 528) the E8M0 codes e + 127 of the 16 blocks of 32
+ * channels.  For each block: e = the smallest exponent with amax <= 448 * 2^e (no
+ * element clips), clamped to [-127, 127] (all-zero block: -127); code_i =
+ * E4M3_rn(x_i / 2^e).  rows: bf16 [n][512]; req/pos: [n] with 0 <= req < n_ring and
+ * pos >= 0 (device-side violations set the error word).  Entries of one call must not
+ * share a slot. */
+csa2_status csa2_pack_window(const void* rows, const int32_t* req, const int64_t* pos, int64_t n, uint8_t* ring,
+                             int32_t n_ring, void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 /* Lightning-indexer scores [P1 "DeepSeek-V3.2" index score, "DeepSeek-V4" the indexer
  * in four bits; P2 "The indexer", "CSA" scorer]:
