@@ -317,7 +317,7 @@ def _timed(csa2, fn, warmup, steps):
     return ms, kernels
 
 
-def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3, sinks_rope=False):
+def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3, sinks_rope=False, ring=False):
     import synth
     mp = (T + 127) // 128
     cache = _device_cache(csa2, dev, B, T - 1, mp, seed, frac)
@@ -335,19 +335,34 @@ def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3, sink
         extra = {"sinks": synth.torch_normal_f32(sb + 7, (HEADS,), dev),
                  "rope_cos": torch.cos(ang).float().expand(B, 32).contiguous(),
                  "rope_sin": torch.sin(ang).float().expand(B, 32).contiguous()}
-    step = csa2.make_step(n_q=B, t_max=T, q=q, req=torch.arange(B, dtype=torch.int32, device=dev),
-                          n_visible=torch.full((B,), T, dtype=torch.int32, device=dev), window=window,
-                          win_start=torch.arange(B, dtype=torch.int64, device=dev) * WIN,
-                          win_len=torch.full((B,), WIN, dtype=torch.int32, device=dev), cache=cache,
-                          topk_idx=torch.empty((B, TOPK), dtype=torch.int32, device=dev), out=out,
-                          lse=torch.empty((B, HEADS), dtype=torch.float32, device=dev), q_idx=q_idx, w=w,
-                          heads_I=HEADS_I, group=1, n_new=B, new_latent=new_lat, new_idx_key=new_key,
-                          new_req=torch.arange(B, dtype=torch.int32, device=dev),
-                          new_pos=torch.full((B,), T - 1, dtype=torch.int64, device=dev), **extra)
+    kw = dict(n_q=B, t_max=T, q=q, req=torch.arange(B, dtype=torch.int32, device=dev),
+              n_visible=torch.full((B,), T, dtype=torch.int32, device=dev), window=window,
+              win_start=torch.arange(B, dtype=torch.int64, device=dev) * WIN,
+              win_len=torch.full((B,), WIN, dtype=torch.int32, device=dev), cache=cache,
+              topk_idx=torch.empty((B, TOPK), dtype=torch.int32, device=dev), out=out,
+              lse=torch.empty((B, HEADS), dtype=torch.float32, device=dev), q_idx=q_idx, w=w,
+              heads_I=HEADS_I, group=1, n_new=B, new_latent=new_lat, new_idx_key=new_key,
+              new_req=torch.arange(B, dtype=torch.int32, device=dev),
+              new_pos=torch.full((B,), T - 1, dtype=torch.int64, device=dev), **extra)
+    step = csa2.make_step(**kw)
     ws = csa2.alloc_workspace(B, HEADS_I, T, True, dev)
-    ms, kernels = _timed(csa2, lambda: csa2.sparse_attn_full(step, ws), warmup, steps)
+    run = lambda: csa2.sparse_attn_full(step, ws)
+    if ring:  # FP8 window ring: the 127 earlier window entries packed once, the step's own each step
+        wring = torch.zeros(B * WIN * 528, dtype=torch.uint8, device=dev)
+        req = torch.arange(B, dtype=torch.int32, device=dev)
+        for j in range(WIN - 1):
+            csa2.pack_window(window[j::WIN].contiguous(), req, torch.full((B,), T - WIN + j, dtype=torch.int64,
+                                                                             device=dev), wring, B, ws)
+        own = window[WIN - 1::WIN].contiguous()
+        own_pos = torch.full((B,), T - 1, dtype=torch.int64, device=dev)
+        step = csa2.make_step(**{**kw, "window": None, "win_ring": wring, "win_ring_reqs": B, "win_start": own_pos})
+
+        def run():
+            csa2.pack_window(own, req, own_pos, wring, B, ws)
+            csa2.sparse_attn_full(step, ws)
+    ms, kernels = _timed(csa2, run, warmup, steps)
     st, info = csa2.check(ws)
-    must = B * (T * 72 + TOPK * 288 + WIN * D * 2)
+    must = B * (T * 72 + TOPK * 288 + WIN * (528 if ring else D * 2))
     return {"workload": name, "metric": UNIT, "value": round(1000.0 / ms, 2), "ms_per_step": round(ms, 4),
             "must_read_bytes": must, "step_gbs": round(must / (ms * 1e-3) / 1e9, 1),
             "index_gbs": round(B * T * 72 / (kernels.get("index", float("nan")) * 1e-6) / 1e9, 1),
@@ -409,6 +424,9 @@ def measure_extra(dev, hbm_peak, bf16_tflops):
     attempt(reuse_reindex)
     attempt(lambda: dict(_decode_line(csa2, dev, "Full decode with per-head sinks and fused partial RoPE, B=64, "
                                       "T=131072", 64, 131072, 3200, sinks_rope=True), note="next row N4"))
+    attempt(lambda: dict(_decode_line(csa2, dev, "Full decode with the FP8 window ring (the step's own window entry "
+                                      "packed each step), B=64, T=131072", 64, 131072, 3300, ring=True),
+                         note="next row N2"))
     attempt(lambda: dict(_decode_line(csa2, dev, "million-token Full decode, B=8, T=1048576, 1% of entries x8", 8,
                                       1 << 20, 3000, 0.01), note="decoder layer"))
     attempt(lambda: dict(_decode_line(csa2, dev, "ratio-2 layer Full decode, B=8, 524288 pooled entries, 1% x8", 8,

@@ -76,6 +76,9 @@ __device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_newest_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
+// kExt: the optional features (sinks, partial RoPE, FP8 window ring) are compiled in;
+// the plain instance carries none of their code.
+template <bool kExt>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,7 +129,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     }
     cp_async_commit();
     const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
-    for (int c = tid; a.win_ring == nullptr && c < 128 * 64; c += kAttnThreads) {  // bf16 window rows
+    const bool bf16_rows = !kExt || a.win_ring == nullptr;
+    for (int c = tid; bf16_rows && c < 128 * 64; c += kAttnThreads) {  // bf16 window rows
       uint32_t r, ch;
       tile_item(static_cast<uint32_t>(c), 128, r, ch);
       const bool ok = static_cast<int32_t>(r) < wl;
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     if (t == 4) {
       if (staged < 4) cp_async_wait_newest_pending();  // queries and window landed; records may still fly
       else cp_async_wait_all();
-      if (a.rope_cos != nullptr) {
+      if (kExt && a.rope_cos != nullptr) {
         // q = q cos + rotate_half(q) sin on channels 448 + i / 480 + i (angle i), in place
         __syncthreads();  // every thread's query pieces have landed
         for (int p = tid; p < kHH * 32; p += kAttnThreads) {
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
           *pb = __float2bfloat16_rn(y * c + x * sn);
         }
       }
-      if (a.win_ring != nullptr) {
+      if (kExt && a.win_ring != nullptr) {
         // FP8 window ring: row i of the tile is the entry of position newest - i, read
         // after the wait on the previous kernel (the ring is written by an earlier call);
         // E4M3 -> f16 in hardware, times the block's 2^e, -> bf16 (exact)
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     if (tid < kHH) {
       const float l = lred[tid] + lred[kHH + tid] + lred[2 * kHH + tid] + lred[3 * kHH + tid];
       float lse2 = -INFINITY, inv = 0.0f;  // log2 sum-exp; O = O^T * inv
-      if (a.sinks == nullptr) {
+      if (!kExt || a.sinks == nullptr) {
         if (l > 0.0f) {
           lse2 = ref[tid] + log2f(l);
           inv = 1.0f / l;
@@ -442,7 +446,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     // tile, then written out with 16-byte coalesced stores
     __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(Kt);
     float* otail = reinterpret_cast<float*>(Ps);  // [32 heads][64] fp32 rotated channels (RoPE)
-    const bool rope = a.rope_cos != nullptr;
+    const bool rope = kExt && a.rope_cos != nullptr;
     for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
       const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
       uint32_t r[32];
@@ -497,10 +501,12 @@ size_t attn_smem_bytes() {
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_q == 0) return cudaSuccess;
   const size_t smem = attn_smem_bytes();
-  static std::atomic<int> limit_set[kMaxDevices];
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(attn_kernel), smem, limit_set);
+  static std::atomic<int> limit_set[2][kMaxDevices];
+  const bool ext = a.sinks != nullptr || a.rope_cos != nullptr || a.win_ring != nullptr;
+  auto* kernel = ext ? attn_kernel<true> : attn_kernel<false>;
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kernel), smem, limit_set[ext ? 1 : 0]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_kernel, dim3(static_cast<unsigned>(2 * a.n_q)), dim3(kAttnThreads), smem, stream, nullptr, a);
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(2 * a.n_q)), dim3(kAttnThreads), smem, stream, nullptr, a);
 }
 
 }  // namespace csa2
