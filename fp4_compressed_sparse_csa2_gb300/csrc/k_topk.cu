@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(const TopkArgs 
 }
 
 // The bin holding the k-th largest key and the number of keys in higher bins.
-// h: smem histogram; 512 threads.
+// h: smem histogram; 512 threads.  Thread t owns bins 4t .. 4t+3; suffix sums run over
+// a warp with shuffles, then over the 16 warp totals in warp 0.
 __device__ void threshold_bin(const uint32_t* h, uint32_t k, int* s_bin, uint32_t* s_above, uint32_t* s_warp) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t loc = h[4 * t] + h[4 * t + 1] + h[4 * t + 2] + h[4 * t + 3];
@@ -80,9 +81,20 @@ __device__ void threshold_bin(const uint32_t* h, uint32_t k, int* s_bin, uint32_
   }
   if (lane == 0) s_warp[warp] = x;
   __syncthreads();
-  uint32_t higher = 0;
-  for (int w = warp + 1; w < kTopkThreads / 32; ++w) higher += s_warp[w];
-  uint32_t running = x - loc + higher;  // keys in bins above 4t+3
+  if (warp == 0) {  // exclusive suffix over the warp totals: keys in the warps above
+    constexpr int kW = kTopkThreads / 32;
+    const uint32_t tot = lane < kW ? s_warp[lane] : 0u;
+    uint32_t y = tot;
+#pragma unroll
+    for (int off = 1; off < kW; off <<= 1) {
+      const uint32_t v = __shfl_down_sync(0xffffffffu, y, off);
+      if (lane + off < kW) y += v;
+    }
+    __syncwarp();
+    if (lane < kW) s_warp[kW + lane] = y - tot;
+  }
+  __syncthreads();
+  uint32_t running = x - loc + s_warp[kTopkThreads / 32 + warp];  // keys in bins above 4t+3
   for (int b = 4 * t + 3; b >= 4 * t; --b) {
     if (running < k && running + h[b] >= k) {
       *s_bin = b;
@@ -485,50 +497,104 @@ __device__ void sort_indices_out(int32_t v, int32_t* runs, int32_t* out, int k) 
 }
 
 // Exact selection among candidate (key, index) pairs that contain the `need` largest
-// keys: three radix levels (11 + 11 + 10 bits) give the key v* of the need-th largest;
-// keys above v* are taken, then the lowest indices among keys equal to v*.  Appends to
-// sel starting at *n_picked.  h: kBins scratch; ties: kBins scratch.  Returns false
-// (nothing written) when the ties at v* do not fit.
+// keys: v* = the need-th largest key, found by radix selection on the key relative to
+// the candidates' smallest key, 8 bits a level from the top of that range (about 3
+// levels: a 256-bin histogram, then one warp finds the digit where the count from the
+// top reaches the remaining need); keys above v* are taken, then the lowest indices
+// among keys equal to v*.  Appends to sel starting at *n_picked.  h: 512 bins scratch
+// (two histograms); ties: kBins scratch.  Returns false (nothing written) when the ties
+// at v* do not fit.
 __device__ bool select_candidates(const uint2* cand, uint32_t nc, uint32_t need, uint32_t* h, int32_t* ties,
-                                  uint32_t* s_warp, int32_t* sel, uint32_t* n_picked, uint32_t* n_ties_ctr) {
-  __shared__ int s_bin;
-  __shared__ uint32_t s_above;
+                                  int32_t* sel, uint32_t* n_picked, uint32_t* n_ties_ctr) {
+  __shared__ uint32_t s_lo, s_hi, s_digit, s_above;
+  constexpr int kPer = kClCandCap / kTopkThreads;  // candidates per thread
+  const uint32_t lane = threadIdx.x & 31;
+  uint32_t key[kPer];
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const uint32_t i = threadIdx.x + j * kTopkThreads;
+    key[j] = i < nc ? cand[i].x : 0u;
+    if (i < nc) {
+      kmin = min(kmin, key[j]);
+      kmax = max(kmax, key[j]);
+    }
+  }
+  if (threadIdx.x == 0) {
+    s_lo = 0xFFFFFFFFu;
+    s_hi = 0u;
+  }
+  for (uint32_t b = threadIdx.x; b < 512u; b += kTopkThreads) h[b] = 0u;  // both level histograms
+  __syncthreads();
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    atomicMin(&s_lo, kmin);
+    atomicMax(&s_hi, kmax);
+  }
+  __syncthreads();
+  const uint32_t base = s_lo, span = s_hi - s_lo;  // relative keys d = key - base lie in [0, span]
+  const int levels = span ? (32 - __clz(span) + 7) / 8 : 0;
   uint32_t prefix = 0, need_l = need;
-  int pbits = 0;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-#pragma unroll 1
-  for (int lv = 0; lv < 3; ++lv) {
-    const int sh = shifts[lv], wd = widths[lv];
-    for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] = 0;
-    __syncthreads();
-    for (uint32_t base = 0; base < nc; base += kTopkThreads) {
-      const uint32_t i = base + threadIdx.x;
-      const uint32_t key = i < nc ? cand[i].x : 0u;
-      const bool in = i < nc && (pbits == 0 || (key >> (32 - pbits)) == prefix);
-      const uint32_t bin = in ? (key >> sh) & ((1u << wd) - 1u) : 0xFFFFFFFFu;
-      // candidates crowd a few bins: one atomic per distinct bin of the warp
-      const uint32_t same = __match_any_sync(0xffffffffu, bin);
-      if (in && (threadIdx.x & 31) == static_cast<uint32_t>(__ffs(same) - 1)) atomicAdd(&h[bin], __popc(same));
+  for (int lv = levels - 1; lv >= 0; --lv) {
+    const int sh = 8 * lv;
+    uint32_t* hc = h + 256 * (lv & 1);                  // this level's histogram (cleared before)
+    uint32_t* hn = h + 256 * ((lv & 1) ^ 1);            // the next level's
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const uint32_t d = key[j] - base;
+      const bool in = threadIdx.x + j * kTopkThreads < nc && (sh + 8 >= 32 || (d >> (sh + 8)) == prefix);
+      if (in) atomicAdd(&hc[(d >> sh) & 255u], 1u);
     }
     __syncthreads();
-    threshold_bin(h, need_l, &s_bin, &s_above, s_warp);
+    if (threadIdx.x < 32) {
+      // lane l owns digits 8l .. 8l+7; counts from the top of the range
+      uint32_t c[8], loc = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        c[b] = hc[8 * lane + b];
+        loc += c[b];
+      }
+      uint32_t x = loc;  // inclusive suffix over lanes
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xffffffffu, x, off);
+        if (lane + off < 32) x += v;
+      }
+      uint32_t running = x - loc;  // keys with a larger digit
+#pragma unroll
+      for (int b = 7; b >= 0; --b) {
+        if (running < need_l && running + c[b] >= need_l) {
+          s_digit = 8 * lane + static_cast<uint32_t>(b);
+          s_above = running;
+        }
+        running += c[b];
+      }
+    } else if (threadIdx.x < 32 + 256) {
+      hn[threadIdx.x - 32] = 0u;
+    }
+    __syncthreads();
+    prefix = (prefix << 8) | s_digit;
     need_l -= s_above;
-    prefix = (prefix << wd) | static_cast<uint32_t>(s_bin);
-    pbits += wd;
   }
-  const uint32_t vstar = prefix, n_ties = h[s_bin];
-  __syncthreads();
-  if (n_ties > static_cast<uint32_t>(kBins)) return false;  // block-uniform
+  const uint32_t vstar = base + prefix;
   const uint32_t start = *n_picked;
   if (threadIdx.x == 0) *n_ties_ctr = 0;
   __syncthreads();
-  for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) {
-    const uint2 c = cand[i];
-    if (c.x > vstar) sel[atomicAdd(n_picked, 1u)] = static_cast<int32_t>(c.y);
-    else if (c.x == vstar) ties[atomicAdd(n_ties_ctr, 1u)] = static_cast<int32_t>(c.y);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const uint32_t i = threadIdx.x + j * kTopkThreads;
+    if (i < nc && key[j] > vstar) {
+      sel[atomicAdd(n_picked, 1u)] = static_cast<int32_t>(cand[i].y);
+    } else if (i < nc && key[j] == vstar) {
+      const uint32_t tslot = atomicAdd(n_ties_ctr, 1u);
+      if (tslot < static_cast<uint32_t>(kBins)) ties[tslot] = static_cast<int32_t>(cand[i].y);
+    }
   }
   __syncthreads();
+  const uint32_t n_ties = *n_ties_ctr;
+  __syncthreads();
+  if (n_ties > static_cast<uint32_t>(kBins)) return false;  // block-uniform
   if (n_ties > 1) {
     int p2 = 1;
     while (p2 < static_cast<int>(n_ties)) p2 <<= 1;
@@ -536,8 +602,8 @@ __device__ bool select_candidates(const uint2* cand, uint32_t nc, uint32_t need,
     __syncthreads();
     bitonic_sort(ties, p2);
   }
-  const uint32_t base = start + (need - need_l);
-  for (uint32_t i = threadIdx.x; i < need_l; i += kTopkThreads) sel[base + i] = ties[i];
+  const uint32_t taken = start + (need - need_l);  // keys above v*
+  for (uint32_t i = threadIdx.x; i < need_l; i += kTopkThreads) sel[taken + i] = ties[i];
   __syncthreads();
   if (threadIdx.x == 0) *n_picked = start + need;
   __syncthreads();
@@ -833,8 +899,8 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
   if (ctr[3] == 0 && nc <= static_cast<uint32_t>(kClCandCap)) {
     if (threadIdx.x == 0) ctr[2] = above;  // entries of higher bins are already in sel[0, above)
     __syncthreads();
-    done = select_candidates(cand, nc, static_cast<uint32_t>(a.k) - above, h, reinterpret_cast<int32_t*>(hsum), s_warp,
-                             sel, &ctr[2], &lctr[3]);
+    done = select_candidates(cand, nc, static_cast<uint32_t>(a.k) - above, h, reinterpret_cast<int32_t*>(hsum), sel,
+                             &ctr[2], &lctr[3]);
   }
   if (!done) full_row_select(a, q, nv, h, s_warp, sel, &ctr[2]);
   sort_indices_out(threadIdx.x < a.k ? sel[threadIdx.x] : INT_MAX, reinterpret_cast<int32_t*>(hsum), out, a.k);
