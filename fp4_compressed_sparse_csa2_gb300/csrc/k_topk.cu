@@ -440,6 +440,12 @@ __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
   asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
   return old;
 }
+__device__ __forceinline__ uint4 dsmem_ld4(uint32_t addr) {  // 16-byte aligned
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -494,6 +500,66 @@ __device__ void sort_indices_out(int32_t v, int32_t* runs, int32_t* out, int k) 
   for (int w = 0; w < kTopkThreads / 32; ++w)
     if (w != warp) pos += lo[w] + (runs[32 * w + lo[w]] < v ? 1 : 0);
   if (pos < k && v != INT_MAX) out[pos] = v;
+}
+
+// Writes the k distinct selected indices of [0, nv) in ascending order: a bitmap of the
+// row; warp w owns a contiguous run of words that its lanes read 32 consecutive words at
+// a time (no bank conflicts); a block prefix over the warps' popcounts, then a warp scan
+// per 32 words gives every set bit its rank.  bm: ceil(nv / 32) words of scratch.
+__device__ void bitmap_indices_out(const int32_t* sel, int k, int64_t nv, uint32_t* bm, uint32_t* s_warp,
+                                   int32_t* out) {
+  constexpr int kW = kTopkThreads / 32;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int W = static_cast<int>((nv + 31) >> 5);
+  const int per_w = (((W + kW - 1) / kW) + 31) & ~31;  // words per warp, a multiple of 32
+  for (int w = t; w < W; w += kTopkThreads) bm[w] = 0u;
+  __syncthreads();
+  for (int i = t; i < k; i += kTopkThreads) {
+    const int32_t v = sel[i];
+    atomicOr(&bm[v >> 5], 1u << (v & 31));
+  }
+  __syncthreads();
+  const int wb = warp * per_w;
+  uint32_t tot = 0;
+  for (int j = 0; j < per_w; j += 32) {
+    const int w = wb + j + lane;
+    tot += w < W ? static_cast<uint32_t>(__popc(bm[w])) : 0u;
+  }
+  tot = __reduce_add_sync(0xffffffffu, tot);
+  if (lane == 0) s_warp[warp] = tot;
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix over the warps
+    const uint32_t v0 = lane < kW ? s_warp[lane] : 0u;
+    uint32_t y = v0;
+#pragma unroll
+    for (int off = 1; off < kW; off <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, y, off);
+      if (lane >= off) y += v;
+    }
+    __syncwarp();
+    if (lane < kW) s_warp[kW + lane] = y - v0;
+  }
+  __syncthreads();
+  uint32_t run = s_warp[kW + warp];
+  for (int j = 0; j < per_w; j += 32) {
+    const int w = wb + j + lane;
+    uint32_t bits = w < W ? bm[w] : 0u;
+    const uint32_t c = static_cast<uint32_t>(__popc(bits));
+    uint32_t incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    uint32_t pos = run + incl - c;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      if (pos < static_cast<uint32_t>(k)) out[pos] = w * 32 + b;
+      ++pos;
+      bits &= bits - 1u;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
 }
 
 // Exact selection among candidate (key, index) pairs that contain the `need` largest
@@ -799,10 +865,17 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
   __syncthreads();
   for (int b = threadIdx.x; b < kBins; b += kTopkThreads) h[b] += h[kBins + b];
   cluster_sync_all();  // every CTA's histogram and the leader's counters are ready
-  for (int b = threadIdx.x; b < kBins; b += kTopkThreads) {
-    uint32_t sum = 0;
-    for (uint32_t r = 0; r < csize; ++r) sum += dsmem_ld(dsmem_map(&h[b], r));
-    hsum[b] = sum;
+  {
+    static_assert(kBins == 4 * kTopkThreads, "one 16-byte histogram slice per thread");
+    uint4 sum = make_uint4(0u, 0u, 0u, 0u);
+    for (uint32_t r = 0; r < csize; ++r) {
+      const uint4 v = dsmem_ld4(dsmem_map(&h[4 * threadIdx.x], r));
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
+    }
+    *reinterpret_cast<uint4*>(&hsum[4 * threadIdx.x]) = sum;
   }
   __syncthreads();
   threshold_bin(hsum, static_cast<uint32_t>(a.k), &s_bin, &s_above, s_warp);
@@ -903,7 +976,11 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
                              &ctr[2], &lctr[3]);
   }
   if (!done) full_row_select(a, q, nv, h, s_warp, sel, &ctr[2]);
-  sort_indices_out(threadIdx.x < a.k ? sel[threadIdx.x] : INT_MAX, reinterpret_cast<int32_t*>(hsum), out, a.k);
+  // ascending output: a bitmap of the row in the free candidate buffer when it fits
+  if (nv <= static_cast<int64_t>(kClCandCap) * 2 * 32)
+    bitmap_indices_out(sel, a.k, nv, reinterpret_cast<uint32_t*>(cand), s_warp, out);
+  else
+    sort_indices_out(threadIdx.x < a.k ? sel[threadIdx.x] : INT_MAX, reinterpret_cast<int32_t*>(hsum), out, a.k);
 }
 
 size_t topk_cluster_smem() {
