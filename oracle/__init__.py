@@ -41,6 +41,8 @@ KV_BYTES = 288   # 256 B nibbles + 32 E4M3 scales [P1 "DeepSeek-V4.1"]
 IDX_BYTES = 72   # 64 B nibbles + 8 E4M3 scales [P3 section 3]
 KV_PAGE_BYTES = PAGE * KV_BYTES
 IDX_PAGE_BYTES = PAGE * IDX_BYTES
+IDX_MX_BYTES = 68  # MXFP4 indexer key: 64 B nibbles + 4 E8M0 scales [P1 "DeepSeek-V4"; P4 "What's in a cell"]
+IDX_MX_PAGE_BYTES = PAGE * IDX_MX_BYTES
 
 
 def build(force: bool = False) -> str:
@@ -101,9 +103,17 @@ def _declare(L):
     L.or_attention_ring.argtypes = [_u16p, ctypes.c_int32, _i32p, ctypes.c_int32, _u8p, _i32p,
                                     ctypes.c_int32, ctypes.c_int32, _u8p, ctypes.c_int64, ctypes.c_int32,
                                     ctypes.c_double, _f64p, _f64p, _f64p, _f64p, _f64p]
+    L.or_mx_exponent.argtypes = [ctypes.c_double]
+    L.or_mx_exponent.restype = ctypes.c_int32
+    L.or_mx_quant_block32.argtypes = [_f32p, _u8p, _u8p]
+    L.or_pack_idx_mx.argtypes = [_u16p, _i32p, _i64p, ctypes.c_int64, _u8p, _i32p, ctypes.c_int32]
+    L.or_read_idx_mx.argtypes = [_u8p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _f64p]
+    L.or_index_score_mx.argtypes = [_u16p, _f32p, ctypes.c_int32, _u8p, _i32p, ctypes.c_int32,
+                                    ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _f64p, _f64p]
     for f in ("or_quant_block16", "or_quant_vector", "or_pack_kv", "or_read_main", "or_read_idx",
               "or_index_score", "or_topk", "or_attention", "or_attention_ext", "or_pack_window",
-              "or_read_window", "or_attention_ring"):
+              "or_read_window", "or_attention_ring", "or_mx_quant_block32", "or_pack_idx_mx",
+              "or_read_idx_mx", "or_index_score_mx"):
         getattr(L, f).restype = None
 
 
@@ -358,3 +368,64 @@ def attention_ring(q_bf16, idx, kv_pages, r, ring, win_pos, win_len, scale=None,
                             None if sk is None else _p(sk, _f64p), None if c is None else _p(c, _f64p),
                             None if s is None else _p(s, _f64p), _p(O, _f64p), _p(lse, _f64p))
     return O, lse
+
+
+# ------------------------------------------------ MXFP4 indexer key [P1][P3][P4]
+
+def mx_exponent(amax: float) -> int:
+    """E8M0 exponent of an MXFP4 block: the smallest e with amax <= 6 * 2^e, clamped to
+    [-127, 127] (-127 for an all-zero block) [P1 precision primer, MX formats and E8M0]."""
+    return int(lib().or_mx_exponent(float(amax)))
+
+
+def mx_quant_block32(x) -> tuple[np.ndarray, int]:
+    """E2M1 codes [32] and E8M0 code (e + 127) of one 32-element MXFP4 block."""
+    xf = np.ascontiguousarray(x, dtype=np.float32)
+    assert xf.shape == (32,)
+    codes = np.zeros(32, np.uint8)
+    sc = np.zeros(1, np.uint8)
+    lib().or_mx_quant_block32(_p(xf, _f32p), _p(codes, _u8p), _p(sc, _u8p))
+    return codes, int(sc[0])
+
+
+def alloc_idx_mx_pages(n_pages: int) -> np.ndarray:
+    """Zeroed MXFP4 indexer-K pages (8704 B = 128 x 68 each)."""
+    return np.zeros(n_pages * IDX_MX_PAGE_BYTES, np.uint8)
+
+
+def pack_idx_mx(idx_key_bf16, req, pos, idx_pages, block_table=None, max_pages=0):
+    """Write n indexer keys (uint16 bf16 bits [n][128]) as 68-byte MXFP4 entries
+    [P1 "DeepSeek-V4"; P4 "What's in a cell": 64 B of nibbles + four E8M0 scales]."""
+    key = np.ascontiguousarray(idx_key_bf16, dtype=np.uint16)
+    req = np.ascontiguousarray(req, dtype=np.int32)
+    pos = np.ascontiguousarray(pos, dtype=np.int64)
+    n = key.shape[0]
+    assert key.shape == (n, DI) and req.shape == (n,) and pos.shape == (n,)
+    bt, btp = _bt(block_table)
+    lib().or_pack_idx_mx(_p(key, _u16p), _p(req, _i32p), _p(pos, _i64p), n, _p(idx_pages, _u8p), btp,
+                         int(max_pages))
+
+
+def read_idx_mx(idx_pages, r, s, block_table=None, max_pages=0) -> np.ndarray:
+    """Dequantised MXFP4 key of entry s of request r: e2m1(code) * 2^(scale code - 127)."""
+    out = np.zeros(DI, np.float64)
+    bt, btp = _bt(block_table)
+    lib().or_read_idx_mx(_p(idx_pages, _u8p), btp, int(max_pages), int(r), int(s), _p(out, _f64p))
+    return out
+
+
+def index_score_mx(q_idx_bf16, w, idx_pages, r, s0, s1, block_table=None, max_pages=0):
+    """index_score over MXFP4 keys with the query quantised to MXFP4 (fp64 sums)."""
+    q = np.ascontiguousarray(q_idx_bf16, dtype=np.uint16)
+    heads = q.shape[0]
+    assert q.shape == (heads, DI)
+    wf = np.ascontiguousarray(w, dtype=np.float32)
+    assert wf.shape == (heads,)
+    n = max(0, int(s1) - int(s0))
+    I = np.zeros(n, np.float64)
+    M = np.zeros(n, np.float64)
+    bt, btp = _bt(block_table)
+    if n:
+        lib().or_index_score_mx(_p(q, _u16p), _p(wf, _f32p), heads, _p(idx_pages, _u8p), btp,
+                                int(max_pages), int(r), int(s0), int(s1), _p(I, _f64p), _p(M, _f64p))
+    return I, M

@@ -21,6 +21,9 @@
  *        visible), "What replaced MLA" (K and V are the same tensor).
  *   [P3] "DeepSeek-V4.1-Flash and the 890-byte KV cache", section 3
  *        (indexer key in the main-KV format: 72 B per entry).
+ *   [P4] "From First Principles: DeepSeek-V4.1-Flash Inference", "What's in a
+ *        cell" (the MXFP4 indexer key: 64 B of nibbles + four E8M0 scales, 68 B;
+ *        see the MXFP4 section at the end of this file).
  *
  * Precision: codecs decide integer codes in fp32 (the kernel's precision);
  * every dot product, score, softmax and output accumulation is fp64.
@@ -480,4 +483,109 @@ void or_attention_ring(const uint16_t* q, int32_t heads, const int32_t* idx, int
   for (int i = 0; i < win_len; ++i, ++t) or_read_window(ring, r, win_pos - i, keys + (int64_t)t * OR_D);
   or_attend(q, heads, keys, nk, scale, sinks, cos_, sin_, O, lse);
   free(keys);
+}
+
+/* ------------------------------------------- MXFP4 indexer key [P1][P3][P4]
+ * "DeepSeek's Attention and KV Cache", "A Precision Primer" (block scaling: MX
+ * formats and E8M0): an MX block is k = 32 elements sharing one E8M0 scale, a pure
+ * power of two 2^-127 .. 2^127, decoded as v_i = X * P_i; MXFP4 takes E2M1 elements
+ * (4 + 8/32 = 4.25 bits each).  "DeepSeek-V4 ... the indexer in four bits" and "From
+ * First Principles: DeepSeek-V4.1-Flash Inference", "What's in a cell": the indexer
+ * key is MXFP4, 64 bytes of nibbles plus four E8M0 scales, 68 bytes.
+ * Scale (the pages fix the format, not the rule): the primer's worked example has a
+ * block maximum of 3 + delta take the scale 1, since E8M0 must round the ideal
+ * (3 + delta)/6 up; so the scale is the smallest power of two 2^e with amax <= 6 * 2^e
+ * (no element clips), e clamped to [-127, 127], e = -127 for an all-zero block.
+ * Element: E2M1 round-to-nearest-even of the exact quotient x / 2^e.
+ * Indexer-K page in this format: 8704 B = 128 * 68: the nibbles of entry e, channel c
+ * where the 72-byte format has them, (e/8)*512 + (c/32)*128 + (e%8)*16 + (c%32)/2;
+ * the E8M0 code e + 127 of entry e, block b (channels [32b, 32b+32)) at
+ * 8192 + (e%32)*16 + (e/32)*4 + b. */
+#define OR_IDX_MX_BYTES 68
+#define OR_IDX_MX_PAGE_BYTES (OR_PAGE * OR_IDX_MX_BYTES)
+
+int32_t or_mx_exponent(double amax) {
+  if (!(amax > 0.0)) return -127;
+  int E;
+  frexp(amax, &E); /* amax in [2^(E-1), 2^E): 6 * 2^(E-4) < 2^(E-1) <= amax < 6 * 2^(E-2) */
+  int e = amax <= ldexp(6.0, E - 3) ? E - 3 : E - 2;
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
+/* One 32-element block: E2M1 codes and the E8M0 code e + 127. */
+void or_mx_quant_block32(const float* x, uint8_t* codes, uint8_t* scale_code) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i) {
+    double a = fabs((double)x[i]);
+    if (a > amax) amax = a;
+  }
+  int e = or_mx_exponent(amax);
+  for (int i = 0; i < 32; ++i) codes[i] = or_e2m1_encode((float)ldexp((double)x[i], -e));
+  *scale_code = (uint8_t)(e + 127);
+}
+
+static int64_t idx_mx_sf_off(int64_t e, int64_t b) { return 8192 + (e % 32) * 16 + (e / 32) * 4 + b; }
+
+/* Pack n indexer keys (bf16 [n][128]) in the MXFP4 format at positions pos[i] of
+ * requests req[i]. */
+void or_pack_idx_mx(const uint16_t* idx_key, const int32_t* req, const int64_t* pos, int64_t n,
+                    uint8_t* idx_pages, const int32_t* bt, int32_t max_pages) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint8_t* pg = idx_pages + page_of(bt, max_pages, req[i], pos[i]) * OR_IDX_MX_PAGE_BYTES;
+    int64_t e = pos[i] % OR_PAGE;
+    for (int b = 0; b < 4; ++b) {
+      float x[32];
+      uint8_t codes[32], sc;
+      for (int c = 0; c < 32; ++c) x[c] = bf16_to_float(idx_key[i * OR_DI + 32 * b + c]);
+      or_mx_quant_block32(x, codes, &sc);
+      for (int c = 0; c < 32; c += 2) pg[idx_nib_off(e, 32 * b + c)] = (uint8_t)(codes[c] | (codes[c + 1] << 4));
+      pg[idx_mx_sf_off(e, b)] = sc;
+    }
+  }
+}
+
+void or_read_idx_mx(const uint8_t* idx_pages, const int32_t* bt, int32_t max_pages, int32_t r, int64_t s,
+                    double* out) {
+  const uint8_t* pg = idx_pages + page_of(bt, max_pages, r, s) * OR_IDX_MX_PAGE_BYTES;
+  int64_t e = s % OR_PAGE;
+  for (int c = 0; c < OR_DI; ++c) {
+    uint8_t byte = pg[idx_nib_off(e, c)];
+    uint8_t code = (c % 2) ? (byte >> 4) : (byte & 15);
+    out[c] = or_e2m1_decode(code) * ldexp(1.0, (int)pg[idx_mx_sf_off(e, c / 32)] - 127);
+  }
+}
+
+/* Index score over MXFP4 keys with the query quantised to MXFP4 too (the query-key
+ * path is FP4 end to end): the same sum as or_index_score, fp64. */
+void or_index_score_mx(const uint16_t* q_idx, const float* w, int32_t heads, const uint8_t* idx_pages,
+                       const int32_t* bt, int32_t max_pages, int32_t r, int64_t s0, int64_t s1, double* I,
+                       double* M) {
+  double* qh = (double*)malloc(sizeof(double) * heads * OR_DI);
+  for (int j = 0; j < heads; ++j) {
+    for (int b = 0; b < 4; ++b) {
+      float x[32];
+      uint8_t codes[32], sc;
+      for (int i = 0; i < 32; ++i) x[i] = bf16_to_float(q_idx[(int64_t)j * OR_DI + 32 * b + i]);
+      or_mx_quant_block32(x, codes, &sc);
+      for (int i = 0; i < 32; ++i) qh[j * OR_DI + 32 * b + i] = or_e2m1_decode(codes[i]) * ldexp(1.0, (int)sc - 127);
+    }
+  }
+  const double scale = 1.0 / sqrt(128.0);
+  double k[OR_DI];
+  for (int64_t s = s0; s < s1; ++s) {
+    or_read_idx_mx(idx_pages, bt, max_pages, r, s, k);
+    double acc = 0.0, accm = 0.0;
+    for (int j = 0; j < heads; ++j) {
+      double dot = 0.0;
+      for (int c = 0; c < OR_DI; ++c) dot += qh[j * OR_DI + c] * k[c];
+      double relu = dot * scale > 0.0 ? dot * scale : 0.0;
+      acc += (double)w[j] * relu;
+      accm += fabs((double)w[j]) * relu;
+    }
+    I[s - s0] = acc;
+    M[s - s0] = accm;
+  }
+  free(qh);
 }
