@@ -272,13 +272,15 @@ def profiled_traffic(summary: str, sources, entries: int):
 
 
 # ----------------------------------------------------------------------------- other workloads
-def _device_cache(csa2, dev, n_req, n_entries, max_pages, seed, frac=0.0):
-    """A paged cache of n_req requests x n_entries seeded entries, packed by the library."""
+def _device_cache(csa2, dev, n_req, n_entries, max_pages, seed, frac=0.0, mx=False):
+    """A paged cache of n_req requests x n_entries seeded entries, packed by the library
+    (mx: MXFP4 68-byte indexer keys)."""
     import synth
     n_pages = n_req * max_pages
     kv = torch.empty(n_pages * csa2.KV_PAGE_BYTES, dtype=torch.uint8, device=dev)
-    idx = torch.empty(n_pages * csa2.IDX_PAGE_BYTES, dtype=torch.uint8, device=dev)
-    cache = csa2.make_cache(kv, idx, max_pages)
+    idx = torch.empty(n_pages * (csa2.IDX_MX_PAGE_BYTES if mx else csa2.IDX_PAGE_BYTES), dtype=torch.uint8,
+                      device=dev)
+    cache = csa2.make_cache(kv, idx, max_pages, idx_format=csa2.IDX_MXFP4 if mx else csa2.IDX_E4M3_16)
     ws0 = csa2.alloc_workspace(1, 64, 0, False, dev)
     pos = torch.arange(n_entries, dtype=torch.int64, device=dev)
     for r in range(n_req):
@@ -317,10 +319,10 @@ def _timed(csa2, fn, warmup, steps):
     return ms, kernels
 
 
-def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3, sinks_rope=False, ring=False):
+def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3, sinks_rope=False, ring=False, mx=False):
     import synth
     mp = (T + 127) // 128
-    cache = _device_cache(csa2, dev, B, T - 1, mp, seed, frac)
+    cache = _device_cache(csa2, dev, B, T - 1, mp, seed, frac, mx)
     sb = seed + 7_000_000
     q = synth.torch_normal_bf16(sb + 1, (B, HEADS, D), dev)
     q_idx = synth.torch_normal_bf16(sb + 2, (B, HEADS_I, DI), dev)
@@ -362,16 +364,18 @@ def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3, sink
             csa2.sparse_attn_full(step, ws)
     ms, kernels = _timed(csa2, run, warmup, steps)
     st, info = csa2.check(ws)
-    must = B * (T * 72 + TOPK * 288 + WIN * (528 if ring else D * 2))
+    key_bytes = 68 if mx else 72
+    must = B * (T * key_bytes + TOPK * 288 + WIN * (528 if ring else D * 2))
     return {"workload": name, "metric": UNIT, "value": round(1000.0 / ms, 2), "ms_per_step": round(ms, 4),
             "must_read_bytes": must, "step_gbs": round(must / (ms * 1e-3) / 1e9, 1),
-            "index_gbs": round(B * T * 72 / (kernels.get("index", float("nan")) * 1e-6) / 1e9, 1),
+            "index_gbs": round(B * T * key_bytes / (kernels.get("index", float("nan")) * 1e-6) / 1e9, 1),
             "kernels_us": kernels, "device_status": st}
 
 
 def measure_extra(dev, hbm_peak, bf16_tflops):
     """The other workloads of the layer, each in its own line: the tiny decode, Reuse and
-    Reindex at 128 x 262,144, the headline decode with sinks and fused partial RoPE, the
+    Reindex at 128 x 262,144, the headline decode with sinks and fused partial RoPE, with the
+    FP8 window ring and with MXFP4 indexer keys, the
     million-token decode with its ratio-2 layer (1 % of entries x 8), and a 4,096-token
     chunked prefill on 262,144 cached entries."""
     import synth
@@ -427,6 +431,8 @@ def measure_extra(dev, hbm_peak, bf16_tflops):
     attempt(lambda: dict(_decode_line(csa2, dev, "Full decode with the FP8 window ring (the step's own window entry "
                                       "packed each step), B=64, T=131072", 64, 131072, 3300, ring=True),
                          note="next row N2"))
+    attempt(lambda: dict(_decode_line(csa2, dev, "Full decode with MXFP4 68-byte indexer keys (E8M0 per 32 "
+                                      "channels), B=64, T=131072", 64, 131072, 3400, mx=True), note="next row N3"))
     attempt(lambda: dict(_decode_line(csa2, dev, "million-token Full decode, B=8, T=1048576, 1% of entries x8", 8,
                                       1 << 20, 3000, 0.01), note="decoder layer"))
     attempt(lambda: dict(_decode_line(csa2, dev, "ratio-2 layer Full decode, B=8, 524288 pooled entries, 1% x8", 8,

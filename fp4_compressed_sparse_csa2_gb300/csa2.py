@@ -17,9 +17,10 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
 # sizes fixed by the pages (mirrors the enum in include/csa2.h)
 D, DI, BLOCK = 512, 128, 16
-KV_BYTES, IDX_BYTES, WIN_BYTES = 288, 72, 528
+KV_BYTES, IDX_BYTES, WIN_BYTES, IDX_MX_BYTES = 288, 72, 528, 68
 TOPK, WIN, HEADS, PAGE = 512, 128, 64, 128
-KV_PAGE_BYTES, IDX_PAGE_BYTES = PAGE * KV_BYTES, PAGE * IDX_BYTES
+KV_PAGE_BYTES, IDX_PAGE_BYTES, IDX_MX_PAGE_BYTES = PAGE * KV_BYTES, PAGE * IDX_BYTES, PAGE * IDX_MX_BYTES
+IDX_E4M3_16, IDX_MXFP4 = 0, 1  # indexer-K formats (csa2_cache.idx_format)
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_DEVICE = range(7)
 TRACE_KINDS = {"pack": 0, "index": 1, "topk_hist": 2, "topk_select": 3, "topk_final": 4, "attn": 5, "topk": 6}
@@ -33,7 +34,7 @@ class Csa2Error(RuntimeError):
 
 class csa2_cache(ctypes.Structure):
     _fields_ = [("kv", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
-                ("max_pages", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
+                ("max_pages", ctypes.c_int32), ("n_pages", ctypes.c_int32), ("idx_format", ctypes.c_int32)]
 
 
 class csa2_step(ctypes.Structure):
@@ -95,11 +96,13 @@ def _check(status: int):
         raise Csa2Error(status, lib.csa2_last_error().decode())
 
 
-def make_cache(kv: torch.Tensor, idx: torch.Tensor, max_pages: int, block_table: torch.Tensor | None = None):
-    """csa2_cache over uint8 page arrays kv [n_pages*36864] and idx [n_pages*9216]."""
+def make_cache(kv: torch.Tensor, idx: torch.Tensor, max_pages: int, block_table: torch.Tensor | None = None,
+               idx_format: int = IDX_E4M3_16):
+    """csa2_cache over uint8 page arrays kv [n_pages*36864] and idx [n_pages*9216]
+    (or [n_pages*8704] with idx_format = IDX_MXFP4)."""
     n_pages = kv.numel() // KV_PAGE_BYTES
-    assert idx.numel() // IDX_PAGE_BYTES == n_pages
-    c = csa2_cache(_ptr(kv), _ptr(idx), _ptr(block_table), int(max_pages), int(n_pages))
+    assert idx.numel() // (IDX_MX_PAGE_BYTES if idx_format == IDX_MXFP4 else IDX_PAGE_BYTES) == n_pages
+    c = csa2_cache(_ptr(kv), _ptr(idx), _ptr(block_table), int(max_pages), int(n_pages), int(idx_format))
     c._keep = (kv, idx, block_table)
     return c
 

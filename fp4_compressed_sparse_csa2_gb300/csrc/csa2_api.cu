@@ -127,7 +127,15 @@ csa2_status check_cache(const csa2_cache* c, bool need_kv, bool need_idx) {
   if (need_idx && (c->idx == nullptr || !aligned(c->idx, 256)))
     return fail(CSA2_ERR_INVALID_ARG, "cache.idx must be a 256-byte aligned device pointer");
   if (c->max_pages <= 0 || c->n_pages <= 0) return fail(CSA2_ERR_INVALID_ARG, "cache.max_pages and cache.n_pages must be positive");
+  if (c->idx_format != CSA2_IDX_E4M3_16 && c->idx_format != CSA2_IDX_MXFP4)
+    return fail(CSA2_ERR_INVALID_ARG, "cache.idx_format must be CSA2_IDX_E4M3_16 or CSA2_IDX_MXFP4 (got %d)", c->idx_format);
   return CSA2_OK;
+}
+
+// Bytes of one packed indexer-query group of N rows: the nibbles, then the scale atoms
+// (two of E4M3 per 16 channels, or one of E8M0 per 32 channels for MXFP4).
+int32_t grp_bytes(int32_t N, const csa2_cache& c) {
+  return N * 64 + (c.idx_format == CSA2_IDX_MXFP4 ? 512 : 1024);
 }
 
 int32_t* err_word(void* ws) { return reinterpret_cast<int32_t*>(ws); }
@@ -148,7 +156,7 @@ csa2_status run_pack(const void* latent, const void* idx_key, const int32_t* req
   a.heads_I = heads_I;
   a.G = G;
   a.N = G * heads_I;
-  a.grp_bytes = a.N * 64 + 1024;
+  a.grp_bytes = grp_bytes(a.N, cache);
   a.n_groups = q_idx ? (n_q + G - 1) / G : 0;
   a.qpack = qpack;
   a.err = err;
@@ -170,7 +178,7 @@ csa2_status run_index(const csa2_cache& cache, const uint8_t* qpack, const float
   a.heads_I = heads_I;
   a.G = G;
   a.N = G * heads_I;
-  a.grp_bytes = a.N * 64 + 1024;
+  a.grp_bytes = grp_bytes(a.N, cache);
   a.w = w;
   a.req = req;
   a.n_visible = n_visible;

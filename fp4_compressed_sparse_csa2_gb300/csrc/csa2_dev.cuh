@@ -214,6 +214,15 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, MX block scaling (scale_vec::2X): E2M1 x E2M1, UE8M0 scale per
+// 32 elements (bit 23).  One 32-bit TMEM scale column holds four block scales of a row;
+// sf_id (bits 29-30 for A, 4-5 for B) names the byte of the first of the two blocks this
+// K = 64 MMA uses: 0 for channels 0-63, 2 for 64-127.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (sf_id << 29);
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
@@ -228,6 +237,16 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a, uint64_t b
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], "
+      "p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], "
       "p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
@@ -329,6 +348,35 @@ __device__ __forceinline__ int e8m0_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
+// MXFP4 block scale: the smallest e with amax <= 6 * 2^e, clamped to [-127, 127]
+// (amax == 0: -127).  amax lies in [2^(E-1), 2^E), so e is E - 3 or E - 2; one exact
+// comparison decides (6 * 2^(E-3) is a normal fp32 wherever the clamp does not apply).
+__device__ __forceinline__ int mx_exponent(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  int E;
+  frexpf(amax, &E);
+  const int e = amax <= ldexpf(6.0f, E - 3) ? E - 3 : E - 2;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Quantise 32 fp32 values to MXFP4: returns the E8M0 code e + 127; writes 16 bytes of
+// nibbles (value 2i in the low nibble of byte i) as four words.
+__device__ __forceinline__ uint32_t quant_block32_mx(const float (&x)[32], uint32_t (&nib)[4]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const int e = mx_exponent(amax);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      v |= cvt_e2m1x2(ldexpf(x[8 * k + 2 * m], -e), ldexpf(x[8 * k + 2 * m + 1], -e)) << (8 * m);  // exact quotients
+    nib[k] = v;
+  }
+  return static_cast<uint32_t>(e + 127);
+}
+
 // Two E4M3 codes (low byte first) -> f16x2, exactly (hardware conversion).
 __device__ __forceinline__ __half2 e4m3x2_f16x2(uint32_t two) {
   uint32_t r;
@@ -393,6 +441,7 @@ constexpr int kD = CSA2_D, kDI = CSA2_DI, kPage = CSA2_PAGE;
 constexpr int kKvBytes = CSA2_KV_BYTES, kKvPageBytes = CSA2_KV_PAGE_BYTES;
 constexpr int kIdxPageBytes = CSA2_IDX_PAGE_BYTES;
 constexpr int kIdxNibBytes = 8192;  // nibble region of an indexer page
+constexpr int kIdxMxPageBytes = CSA2_IDX_MX_PAGE_BYTES;
 
 __device__ __forceinline__ int64_t page_id(const csa2_cache& c, int32_t r, int64_t s) {
   const int64_t j = s / kPage;
@@ -407,6 +456,11 @@ __device__ __forceinline__ uint32_t idx_nib_off(uint32_t n, uint32_t b) {
 }
 __device__ __forceinline__ uint32_t idx_sf_off(uint32_t nib_bytes, uint32_t n, uint32_t b) {
   return nib_bytes + (b >> 2) * 512u + (n & 31u) * 16u + (n >> 5) * 4u + (b & 3u);
+}
+
+// MXFP4 scale byte of row n, 32-channel block b (one 512-byte atom holds all four).
+__device__ __forceinline__ uint32_t idx_mx_sf_off(uint32_t nib_bytes, uint32_t n, uint32_t b) {
+  return nib_bytes + (n & 31u) * 16u + (n >> 5) * 4u + b;
 }
 
 }  // namespace csa2

@@ -13,7 +13,9 @@
 //               adjacent pages, plus one per packed query group;
 //   warps 1-4   TMEM allocator (warp 1) and four MMA issuers: tcgen05.cp of the E4M3 scale
 //               atoms into double-buffered TMEM slots as soon as a page lands, then, once
-//               the accumulator is free, two tcgen05.mma kind::mxf4nvf4 (K = 64 each) into
+//               the accumulator is free, two tcgen05.mma kind::mxf4nvf4 (K = 64 each; MX
+//               scale_vec::2X with E8M0 scales per 32 for MXFP4 pages, 4X with E4M3 per 16
+//               otherwise) into
 //               one of 4 (N <= 64) or 2 (N = 128) fp32 TMEM accumulators D[128 keys][N];
 //   warps 5..20 four epilogue warpgroups taking every fourth tile: tcgen05.ld of one TMEM
 //               row per thread (thread = key), 32 columns at a time; the accumulator goes
@@ -70,13 +72,16 @@ __device__ __forceinline__ int64_t seg_page(const Segment& sg, int32_t t) {
 }
 
 // kSplit: N = 128 (two queries of 64 heads per group), handled by warpgroup pairs.
-template <bool kSplit>
+// kMx: MXFP4 pages (8704 B, one E8M0 scale per 32 channels, MX block-scaled MMA);
+// otherwise 9216-byte pages with one E4M3 scale per 16 channels.
+template <bool kSplit, bool kMx>
 __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int S = kIdxStages;
-  uint8_t* ring = smem;                                                 // S x 9216
-  uint8_t* qslot = ring + static_cast<size_t>(S) * kIdxPageBytes;       // 2 x 9216
+  constexpr uint32_t kPg = kMx ? kIdxMxPageBytes : kIdxPageBytes;  // bytes per page
+  uint8_t* ring = smem;                                                 // S x kPg
+  uint8_t* qslot = ring + static_cast<size_t>(S) * kPg;                 // 2 x 9216
   float* sw_all = reinterpret_cast<float*>(qslot + 2 * kIdxPageBytes);  // per epilogue warp: 128 head weights
   uint64_t* bars = reinterpret_cast<uint64_t*>(sw_all + 4 * kEpiGroups * 128);
   uint64_t* full = bars;               // [S]
@@ -173,14 +178,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
-        uint8_t* dst = ring + (k * n_iss + in_st) * kIdxPageBytes;
+        uint8_t* dst = ring + (k * n_iss + in_st) * kPg;
         if (sg.bt_row == nullptr) {
           if (lane == 0) {
             const int64_t page = sg.page_base + t;
             if (page >= 0 && page + cnt <= a.cache.n_pages) {
-              const uint32_t bytes = static_cast<uint32_t>(cnt) * static_cast<uint32_t>(kIdxPageBytes);
+              const uint32_t bytes = static_cast<uint32_t>(cnt) * kPg;
               mbar_expect_tx(&full[k], bytes);
-              bulk_g2s_hint(dst, a.idx_pages + page * kIdxPageBytes, bytes, &full[k], pol);
+              bulk_g2s_hint(dst, a.idx_pages + page * kPg, bytes, &full[k], pol);
             } else {
               report(a.err, CSA2_ERR_DEVICE, kInfoPage);
             }
@@ -188,9 +193,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         } else if (lane < cnt) {
           const int64_t page = __ldg(sg.bt_row + t + lane);
           if (page >= 0 && page < a.cache.n_pages) {
-            mbar_expect_tx(&full[k], static_cast<uint32_t>(kIdxPageBytes));
-            bulk_g2s_hint(dst + lane * kIdxPageBytes, a.idx_pages + page * kIdxPageBytes,
-                          static_cast<uint32_t>(kIdxPageBytes), &full[k], pol);
+            mbar_expect_tx(&full[k], kPg);
+            bulk_g2s_hint(dst + lane * kPg, a.idx_pages + page * kPg, kPg, &full[k], pol);
           } else {
             report(a.err, CSA2_ERR_DEVICE, kInfoPage);
           }
@@ -230,6 +234,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
       // the copy ring moving
       const uint32_t me = static_cast<uint32_t>(warp - 1);
       const uint32_t idesc = idesc_nvf4(128, a.N);
+      const uint32_t idesc_mx[2] = {idesc_mxf4(128, a.N, 0u), idesc_mxf4(128, a.N, 2u)};
       const uint32_t lg_iss = n_iss == 4u ? 2u : (n_iss == 2u ? 1u : 0u);
       const uint32_t lg_st = kLgStages - lg_iss, lg_acc = n_acc == 4 ? 2u : 1u;
       uint32_t n = 0, m = 0, cur = 0;
@@ -245,7 +250,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         const uint32_t qs = smem_u32(qslot + cur * kIdxPageBytes);
         const uint32_t sfb = tmem + 320u + 16u * me + 8u * cur;  // 320..383
         tmem_cp_sf(sfb, sdesc(qs + nib_q, 128, 128));
-        tmem_cp_sf(sfb + 4, sdesc(qs + nib_q + 512, 128, 128));
+        if (!kMx) tmem_cp_sf(sfb + 4, sdesc(qs + nib_q + 512, 128, 128));
         ++m;
         // CTA-local tiles n .. n + len - 1 belong to this segment; this issuer's are the
         // ones with nn % n_iss == me
@@ -257,17 +262,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
           ok = mbar_wait(&full[s], ph, abort);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t st = smem_u32(ring + (s * n_iss + me) * kIdxPageBytes);
+          const uint32_t st = smem_u32(ring + (s * n_iss + me) * kPg);
           const uint32_t sfa = tmem + 256u + 16u * b + 8u * bph;  // 256..319
           tmem_cp_sf(sfa, sdesc(st + kIdxNibBytes, 128, 128));
-          tmem_cp_sf(sfa + 4, sdesc(st + kIdxNibBytes + 512, 128, 128));
+          if (!kMx) tmem_cp_sf(sfa + 4, sdesc(st + kIdxNibBytes + 512, 128, 128));
           ok = mbar_wait(&acc_empty[b], bph ^ 1u, abort);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t kk = 0; kk < 2; ++kk)
-            mma_nvf4(tmem + b * N, sdesc(st + kk * 256u, 128, 512), sdesc(qs + kk * 256u, 128, 512), idesc,
-                     sfa + 4u * kk, sfb + 4u * kk, kk);
+          for (uint32_t kk = 0; kk < 2; ++kk) {
+            if (kMx)  // one scale column per row; the two K halves use its bytes 0-1 and 2-3
+              mma_mxf4(tmem + b * N, sdesc(st + kk * 256u, 128, 512), sdesc(qs + kk * 256u, 128, 512),
+                       idesc_mx[kk], sfa, sfb, kk);
+            else
+              mma_nvf4(tmem + b * N, sdesc(st + kk * 256u, 128, 512), sdesc(qs + kk * 256u, 128, 512), idesc,
+                       sfa + 4u * kk, sfb + 4u * kk, kk);
+          }
           mma_commit(&empty[s]);
           mma_commit(&acc_full[b]);
         }
@@ -378,10 +388,12 @@ size_t index_smem_bytes(int stages) {
 
 cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream) {
   const size_t smem = index_smem_bytes(a.stages);
-  static std::atomic<int> limit_set[2][kMaxDevices];
-  const bool split = a.N == 128;
-  auto* kernel = split ? index_kernel<true> : index_kernel<false>;
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kernel), smem, limit_set[split ? 1 : 0]);
+  static std::atomic<int> limit_set[4][kMaxDevices];
+  const bool split = a.N == 128, mx = a.cache.idx_format == CSA2_IDX_MXFP4;
+  auto* kernel = mx ? (split ? index_kernel<true, true> : index_kernel<false, true>)
+                    : (split ? index_kernel<true, false> : index_kernel<false, false>);
+  cudaError_t e =
+      smem_limit_once(reinterpret_cast<const void*>(kernel), smem, limit_set[(split ? 1 : 0) + (mx ? 2 : 0)]);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kIdxThreads), smem, stream, nullptr, a);
 }

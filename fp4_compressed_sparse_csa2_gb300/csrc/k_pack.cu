@@ -6,11 +6,14 @@
 // entry.  "DeepSeek-V4.1-Flash and the 890-byte KV cache", section 3: the 128-channel
 // indexer key in the same format, 72 B.  "DeepSeek-V4: ... The indexer in four bits":
 // the indexer query-key product runs entirely in FP4, so the query is packed with the
-// same codec.
+// same codec.  Alternatively ("A Precision Primer", MX formats and E8M0; "What's in a
+// cell" of "From First Principles: DeepSeek-V4.1-Flash Inference") the indexer key and
+// query take MXFP4, one power-of-two E8M0 scale per 32 channels, 68 B per key.
 //
 // One thread per 16-channel block: two 16-byte loads, one fp32 division for the
 // scale, 16 for the codes (hardware RN/satfinite conversions), an 8-byte nibble
-// store and a 1-byte scale store.
+// store and a 1-byte scale store.  An MXFP4 block of 32 channels takes one thread:
+// its exponent, 32 exact power-of-two quotients, two 8-byte stores and a scale byte.
 #include "csa2_kernels.cuh"
 
 namespace csa2 {
@@ -57,6 +60,18 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
       uint8_t* rec = a.cache.kv + p * kKvPageBytes + static_cast<int64_t>(e) * kKvBytes;
       *reinterpret_cast<uint2*>(rec + 8 * b) = make_uint2(lo, hi);
       rec[256 + b] = static_cast<uint8_t>(sc);
+    } else if (a.cache.idx_format == CSA2_IDX_MXFP4) {
+      const int bb = b - 32;  // items 32..35: one 32-channel MXFP4 block each
+      if (bb >= 4) return;
+      float x32[32];
+      load16(a.idx_key + i * kDI + 32 * bb, *reinterpret_cast<float(*)[16]>(&x32[0]));
+      load16(a.idx_key + i * kDI + 32 * bb + 16, *reinterpret_cast<float(*)[16]>(&x32[16]));
+      uint32_t nib[4];
+      const uint32_t sc = quant_block32_mx(x32, nib);
+      uint8_t* pg = a.cache.idx + p * kIdxMxPageBytes;
+      *reinterpret_cast<uint2*>(pg + idx_nib_off(e, 2 * bb)) = make_uint2(nib[0], nib[1]);
+      *reinterpret_cast<uint2*>(pg + idx_nib_off(e, 2 * bb + 1)) = make_uint2(nib[2], nib[3]);
+      pg[idx_mx_sf_off(kIdxNibBytes, e, bb)] = static_cast<uint8_t>(sc);
     } else {
       const int bb = b - 32;
       load16(a.idx_key + i * kDI + 16 * bb, x);
@@ -74,6 +89,27 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
   const uint32_t bb = static_cast<uint32_t>(qi % 8);
   uint8_t* gp = a.qpack + g * a.grp_bytes;
   const uint32_t nib_bytes = static_cast<uint32_t>(a.N) * 64u;
+  if (a.cache.idx_format == CSA2_IDX_MXFP4) {  // items bb < 4: one 32-channel block each
+    if (bb >= 4) return;
+    if (n >= static_cast<uint32_t>(a.N)) {
+      gp[idx_mx_sf_off(nib_bytes, n, bb)] = 0;
+      return;
+    }
+    const int64_t q = g * a.G + n / a.heads_I;
+    const int32_t j = static_cast<int32_t>(n % a.heads_I);
+    uint32_t nib[4] = {0u, 0u, 0u, 0u}, sc = 0;
+    if (q < a.n_q) {
+      float x32[32];
+      const __nv_bfloat16* src = a.q_idx + (q * a.heads_I + j) * kDI + 32 * bb;
+      load16(src, *reinterpret_cast<float(*)[16]>(&x32[0]));
+      load16(src + 16, *reinterpret_cast<float(*)[16]>(&x32[16]));
+      sc = quant_block32_mx(x32, nib);
+    }
+    *reinterpret_cast<uint2*>(gp + idx_nib_off(n, 2 * bb)) = make_uint2(nib[0], nib[1]);
+    *reinterpret_cast<uint2*>(gp + idx_nib_off(n, 2 * bb + 1)) = make_uint2(nib[2], nib[3]);
+    gp[idx_mx_sf_off(nib_bytes, n, bb)] = static_cast<uint8_t>(sc);
+    return;
+  }
   if (n >= static_cast<uint32_t>(a.N)) {  // unused scale slots of a short group
     gp[idx_sf_off(nib_bytes, n, bb)] = 0;
     return;

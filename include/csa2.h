@@ -77,8 +77,24 @@ enum {
   CSA2_PAGE = 128,
   CSA2_KV_PAGE_BYTES = 36864,  /* 128 x 288 */
   CSA2_IDX_PAGE_BYTES = 9216,  /* 128 x 72  */
-  CSA2_WIN_BYTES = 528
+  CSA2_WIN_BYTES = 528,
+  CSA2_IDX_MX_BYTES = 68,        /* MXFP4 indexer key: 64 B of nibbles + 4 E8M0 scales */
+  CSA2_IDX_MX_PAGE_BYTES = 8704  /* 128 x 68 */
 };
+
+/* Indexer-K formats (csa2_cache.idx_format).
+ *   CSA2_IDX_E4M3_16  E2M1 with one E4M3 scale per 16 channels, 72 B per entry: the
+ *                     main-KV format [P3 section 3].
+ *   CSA2_IDX_MXFP4    MXFP4: E2M1 with one E8M0 (power-of-two) scale per 32 channels,
+ *                     68 B per entry [P1 "A Precision Primer", MX formats and E8M0;
+ *                     P1 "DeepSeek-V4", the indexer in four bits; P4 "What's in a cell"].
+ *                     Scale 2^e with e the smallest exponent such that the block maximum
+ *                     is <= 6 * 2^e (no element clips; the primer's worked example has a
+ *                     maximum of 3 + delta take the scale 1), clamped to [-127, 127], -127
+ *                     for an all-zero block; code_i = E2M1_rn(x_i / 2^e), exact quotient.
+ *                     The indexer query is quantised in the same format, and the product
+ *                     runs on the MX block-scaled FP4 tensor cores. */
+enum { CSA2_IDX_E4M3_16 = 0, CSA2_IDX_MXFP4 = 1 };
 
 /* The global cache of one CSA2 Full layer: a paged main-KV cache and a paged
  * indexer-K cache sharing one block table [P1 "DeepSeek-V4": compressed entries are a
@@ -97,13 +113,18 @@ enum {
  *   block-scaled tensor-core MMA, so a page feeds the MMA without reshuffling.  The
  *   E4M3 scale of entry e, block b sits at byte 8192 + (b/4)*512 + (e%32)*16 +
  *   (e/32)*4 + b%4, the scale-factor layout the MMA reads.
- * Each entry still costs exactly 288 + 72 bytes. */
+ * Each entry still costs exactly 288 + 72 bytes.
+ * MXFP4 indexer-K page (idx_format = CSA2_IDX_MXFP4; 8704 B = 128 x 68): the nibbles as
+ *   above; the E8M0 code e + 127 of entry e, block b (channels [32b, 32b+32)) at byte
+ *   8192 + (e%32)*16 + (e/32)*4 + b.  Each entry costs 288 + 68 bytes. */
 typedef struct csa2_cache {
   uint8_t* kv;                /* main-KV pages [n_pages][36864]                     */
-  uint8_t* idx;               /* indexer-K pages [n_pages][9216]                    */
+  uint8_t* idx;               /* indexer-K pages [n_pages][9216], or [n_pages][8704]
+                                 with idx_format = CSA2_IDX_MXFP4                  */
   const int32_t* block_table; /* [n_req][max_pages] page ids, or NULL (contiguous)  */
   int32_t max_pages;          /* pages per request (row length of block_table)      */
   int32_t n_pages;            /* pages allocated in kv and idx (bounds check)       */
+  int32_t idx_format;         /* CSA2_IDX_E4M3_16 (0, default) or CSA2_IDX_MXFP4    */
 } csa2_cache;
 
 /* One CSA2 layer step for n_q queries [P1 "DeepSeek-V4.1" three modes; P3 section 2;
@@ -172,7 +193,9 @@ size_t csa2_workspace_bytes(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t
  * P3 section 3].  For each 16-channel block: amax = max|x|, scale =
  * E4M3_rn_satfinite(amax / 6) (fp32 division), code_i = E2M1_rn_satfinite(x_i / scale)
  * (fp32 division; a zero scale gives +0 codes).  latent: bf16 [n][512]; idx_key: bf16
- * [n][128]; req/pos: [n].  Entries at the same (req, pos) must not repeat in one call. */
+ * [n][128]; req/pos: [n].  Entries at the same (req, pos) must not repeat in one call.
+ * With cache->idx_format = CSA2_IDX_MXFP4 the indexer key takes the MXFP4 format
+ * (see CSA2_IDX_MXFP4); the main-KV entry is unchanged. */
 csa2_status csa2_pack_kv(const void* latent, const void* idx_key, const int32_t* req,
                          const int64_t* pos, int64_t n, const csa2_cache* cache, void* ws,
                          size_t ws_bytes, csa2_stream_t stream);
@@ -196,6 +219,8 @@ csa2_status csa2_pack_window(const void* rows, const int32_t* req, const int64_t
  * for s < n_visible[q], where qhat is q_idx quantised in-call with the same E2M1/E4M3
  * block codec and khat the cached indexer key (the product runs on the block-scaled
  * FP4 tensor cores, fp32 accumulation).  Entries s >= n_visible[q] are not written.
+ * With cache->idx_format = CSA2_IDX_MXFP4, qhat and khat are MXFP4 (E8M0 scale per 32
+ * channels) and the product runs as the MX block-scaled MMA.
  * group = 1 or 2 consecutive queries of one request per MMA tile. */
 csa2_status csa2_index_score(const void* q_idx, const float* w, int32_t heads_I,
                              const int32_t* req, const int32_t* n_visible, int64_t n_q,

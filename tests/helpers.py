@@ -24,15 +24,18 @@ def dev(a: np.ndarray) -> torch.Tensor:
 class Cache:
     """A paged cache on the GPU plus its host twin written by the oracle from the same inputs."""
 
-    def __init__(self, n_req: int, max_pages: int, block_table: np.ndarray | None = None, n_pages: int | None = None):
+    def __init__(self, n_req: int, max_pages: int, block_table: np.ndarray | None = None, n_pages: int | None = None,
+                 mx: bool = False):
         from fp4_compressed_sparse_csa2_gb300 import csa2
-        self.n_req, self.max_pages = n_req, max_pages
+        self.n_req, self.max_pages, self.mx = n_req, max_pages, mx
         self.n_pages = n_pages or (n_req * max_pages if block_table is None else int(block_table.max()) + 1)
         self.kv = torch.zeros(self.n_pages * csa2.KV_PAGE_BYTES, dtype=torch.uint8, device="cuda")
-        self.idx = torch.zeros(self.n_pages * csa2.IDX_PAGE_BYTES, dtype=torch.uint8, device="cuda")
+        idx_page = csa2.IDX_MX_PAGE_BYTES if mx else csa2.IDX_PAGE_BYTES
+        self.idx = torch.zeros(self.n_pages * idx_page, dtype=torch.uint8, device="cuda")
         self.bt_np = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
         self.bt = None if block_table is None else dev(self.bt_np)
-        self.c = csa2.make_cache(self.kv, self.idx, max_pages, self.bt)
+        self.c = csa2.make_cache(self.kv, self.idx, max_pages, self.bt,
+                                 idx_format=csa2.IDX_MXFP4 if mx else csa2.IDX_E4M3_16)
         self.ws = csa2.alloc_workspace(1, 64, 0, False)
 
     def pack(self, lat_bits, key_bits, req, pos):
