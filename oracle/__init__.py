@@ -110,10 +110,14 @@ def _declare(L):
     L.or_read_idx_mx.argtypes = [_u8p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _f64p]
     L.or_index_score_mx.argtypes = [_u16p, _f32p, ctypes.c_int32, _u8p, _i32p, ctypes.c_int32,
                                     ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _f64p, _f64p]
+    L.or_block_pool.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i32p]
+    L.or_block_pool.restype = ctypes.c_int64
+    L.or_index_score_at.argtypes = [_u16p, _f32p, ctypes.c_int32, _u8p, _i32p, ctypes.c_int32, ctypes.c_int32,
+                                    _i32p, ctypes.c_int64, ctypes.c_int32, _f64p, _f64p]
     for f in ("or_quant_block16", "or_quant_vector", "or_pack_kv", "or_read_main", "or_read_idx",
               "or_index_score", "or_topk", "or_attention", "or_attention_ext", "or_pack_window",
               "or_read_window", "or_attention_ring", "or_mx_quant_block32", "or_pack_idx_mx",
-              "or_read_idx_mx", "or_index_score_mx"):
+              "or_read_idx_mx", "or_index_score_mx", "or_index_score_at"):
         getattr(L, f).restype = None
 
 
@@ -429,3 +433,44 @@ def index_score_mx(q_idx_bf16, w, idx_pages, r, s0, s1, block_table=None, max_pa
         lib().or_index_score_mx(_p(q, _u16p), _p(wf, _f32p), heads, _p(idx_pages, _u8p), btp,
                                 int(max_pages), int(r), int(s0), int(s1), _p(I, _f64p), _p(M, _f64p))
     return I, M
+
+
+# ------------------------------------------ hierarchical sparse indexer [P1][P4]
+POOL_BLOCK = 8       # positions per block [P1 "The hierarchical indexer"]
+POOL_BLOCKS = 2048   # blocks kept
+POOL = POOL_BLOCK * POOL_BLOCKS
+
+
+def block_pool(scores, n_visible: int, block: int = POOL_BLOCK, keep: int = POOL_BLOCKS) -> tuple[np.ndarray, int]:
+    """Candidate pool of a Full layer's score row: the visible positions of the `keep`
+    blocks of `block` positions with the largest block maxima (ties -> lower block),
+    ascending, -1 padded to keep * block; and their count [P1 "The hierarchical indexer";
+    P4 "The Hierarchical Sparse Indexer"]."""
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    assert s.size >= n_visible
+    pool = np.zeros(keep * block, np.int32)
+    n = lib().or_block_pool(_p(s, _f32p), int(n_visible), int(block), int(keep), _p(pool, _i32p))
+    return pool, int(n)
+
+
+def index_score_at(q_idx_bf16, w, idx_pages, r, positions, mx=False, block_table=None, max_pages=0):
+    """index_score (or index_score_mx) at the listed positions of request r."""
+    q = np.ascontiguousarray(q_idx_bf16, dtype=np.uint16)
+    heads = q.shape[0]
+    wf = np.ascontiguousarray(w, dtype=np.float32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    I = np.zeros(pos.size, np.float64)
+    M = np.zeros(pos.size, np.float64)
+    bt, btp = _bt(block_table)
+    if pos.size:
+        lib().or_index_score_at(_p(q, _u16p), _p(wf, _f32p), heads, _p(idx_pages, _u8p), btp, int(max_pages),
+                                int(r), _p(pos, _i32p), pos.size, int(bool(mx)), _p(I, _f64p), _p(M, _f64p))
+    return I, M
+
+
+def pool_topk(pool_scores, pool, n: int, k: int = 512) -> np.ndarray:
+    """A Reindex layer's own top-k inside the pool: the k largest of the pool's scores
+    (slot i scores position pool[i]; ties -> lower position, as the pool is ascending),
+    returned as positions ascending, -1 padded [P4 "The Hierarchical Sparse Indexer"]."""
+    slots = topk(np.ascontiguousarray(pool_scores, dtype=np.float32)[:n], k)
+    return np.where(slots >= 0, np.asarray(pool)[np.maximum(slots, 0)], -1).astype(np.int32)

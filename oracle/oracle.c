@@ -589,3 +589,64 @@ void or_index_score_mx(const uint16_t* q_idx, const float* w, int32_t heads, con
   }
   free(qh);
 }
+
+/* ----------------------------------------- hierarchical sparse indexer [P1][P4]
+ * "DeepSeek's Attention and KV Cache", "The hierarchical indexer", and "From First
+ * Principles: DeepSeek-V4.1-Flash Inference", "The Hierarchical Sparse Indexer": the
+ * Full layer, besides its own top-512, gives every block of 8 consecutive positions the
+ * maximum score inside it, keeps at most the 2,048 highest-scoring blocks and publishes
+ * their positions (at most 2,048 x 8 = 16,384) as a candidate pool; the Reindex layers
+ * score only the pool and take their own top-512 from inside it.
+ * Readings (the pages are silent): block j covers positions [8j, 8j + 8) that are
+ * visible (s < n_visible); equal block maxima prefer the lower block (the top-k's
+ * lower-index rule), -0 equals +0; the pool lists the positions in ascending order,
+ * -1 after the last. */
+typedef struct {
+  double v;
+  int64_t j;
+} or_blk;
+
+static int cmp_blk(const void* a, const void* b) {
+  const or_blk* x = (const or_blk*)a;
+  const or_blk* y = (const or_blk*)b;
+  if (x->v != y->v) return x->v > y->v ? -1 : 1;
+  return x->j < y->j ? -1 : (x->j > y->j);
+}
+
+/* pool: [keep * block] positions ascending, -1 padded; returns the number listed. */
+int64_t or_block_pool(const float* scores, int64_t nv, int32_t block, int32_t keep, int32_t* pool) {
+  int64_t nb = (nv + block - 1) / block;
+  or_blk* b = (or_blk*)malloc(sizeof(or_blk) * (nb > 0 ? nb : 1));
+  for (int64_t j = 0; j < nb; ++j) {
+    double m = -INFINITY;
+    for (int64_t s = j * block; s < (j + 1) * block && s < nv; ++s)
+      if ((double)scores[s] > m) m = (double)scores[s];
+    b[j].v = m == 0.0 ? 0.0 : m; /* -0 -> +0 */
+    b[j].j = j;
+  }
+  qsort(b, (size_t)nb, sizeof(or_blk), cmp_blk);
+  int64_t take = nb < keep ? nb : keep;
+  uint8_t* sel = (uint8_t*)calloc((size_t)(nb > 0 ? nb : 1), 1);
+  for (int64_t i = 0; i < take; ++i) sel[b[i].j] = 1;
+  int64_t n = 0;
+  for (int64_t j = 0; j < nb; ++j)
+    if (sel[j])
+      for (int64_t s = j * block; s < (j + 1) * block && s < nv; ++s) pool[n++] = (int32_t)s;
+  for (int64_t i = n; i < (int64_t)keep * block; ++i) pool[i] = -1;
+  free(sel);
+  free(b);
+  return n;
+}
+
+/* Index scores at the listed positions (n of them, each < the request's cache length)
+ * of request r; mx selects the MXFP4 key format.  The same sums as or_index_score. */
+void or_index_score_at(const uint16_t* q_idx, const float* w, int32_t heads, const uint8_t* idx_pages,
+                       const int32_t* bt, int32_t max_pages, int32_t r, const int32_t* pos, int64_t n, int32_t mx,
+                       double* I, double* M) {
+  for (int64_t i = 0; i < n; ++i) {
+    if (mx)
+      or_index_score_mx(q_idx, w, heads, idx_pages, bt, max_pages, r, pos[i], pos[i] + 1, I + i, M + i);
+    else
+      or_index_score(q_idx, w, heads, idx_pages, bt, max_pages, r, pos[i], pos[i] + 1, I + i, M + i);
+  }
+}
