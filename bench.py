@@ -433,6 +433,42 @@ def measure_extra(dev, hbm_peak, bf16_tflops):
                          note="next row N2"))
     attempt(lambda: dict(_decode_line(csa2, dev, "Full decode with MXFP4 68-byte indexer keys (E8M0 per 32 "
                                       "channels), B=64, T=131072", 64, 131072, 3400, mx=True), note="next row N3"))
+    def hierarchical():
+        # a Full layer that also publishes its candidate pool, then a Reindex layer that
+        # scores only the pool (16,384 positions) with its own query
+        B, T = 64, 131072
+        mp = T // 128
+        cache = _device_cache(csa2, dev, B, T, mp, 3500)
+        sb = 3500 + 7_000_000
+        common = dict(n_q=B, t_max=T, q=synth.torch_normal_bf16(sb + 1, (B, HEADS, D), dev),
+                      req=torch.arange(B, dtype=torch.int32, device=dev),
+                      n_visible=torch.full((B,), T, dtype=torch.int32, device=dev),
+                      window=synth.torch_normal_bf16(sb + 6, (B * WIN, D), dev),
+                      win_start=torch.arange(B, dtype=torch.int64, device=dev) * WIN,
+                      win_len=torch.full((B,), WIN, dtype=torch.int32, device=dev), cache=cache,
+                      topk_idx=torch.empty((B, TOPK), dtype=torch.int32, device=dev),
+                      out=torch.empty((B, HEADS, D), dtype=torch.bfloat16, device=dev),
+                      lse=torch.empty((B, HEADS), dtype=torch.float32, device=dev), heads_I=HEADS_I)
+        pool = torch.empty((B, csa2.POOL), dtype=torch.int32, device=dev)
+        ws = csa2.alloc_workspace(B, HEADS_I, T, True, dev, pool=True)
+        full = csa2.make_step(q_idx=synth.torch_normal_bf16(sb + 2, (B, HEADS_I, DI), dev),
+                              w=synth.torch_normal_f32(sb + 3, (B, HEADS_I), dev), pool=pool, **common)
+        ms_f, k_f = _timed(csa2, lambda: csa2.sparse_attn_full(full, ws), 3, 10)
+        reidx = csa2.make_step(q_idx=synth.torch_normal_bf16(sb + 4, (B, HEADS_I, DI), dev),
+                               w=synth.torch_normal_f32(sb + 5, (B, HEADS_I), dev), pool=pool, **common)
+        ms_r, k_r = _timed(csa2, lambda: csa2.sparse_attn_reindex(reidx, ws), 3, 20)
+        st, _ = csa2.check(ws)
+        must_r = B * (csa2.POOL * 72 + TOPK * 288 + WIN * D * 2)
+        return {"workload": "hierarchical indexer, B=64, T=131072: Full publishing its 16,384-position pool, "
+                            "then a Reindex over the pool", "metric": UNIT,
+                "full_with_pool": {"value": round(1000.0 / ms_f, 2), "ms_per_step": round(ms_f, 4),
+                                   "kernels_us": k_f},
+                "reindex_over_pool": {"value": round(1000.0 / ms_r, 2), "ms_per_step": round(ms_r, 4),
+                                      "kernels_us": k_r, "must_read_bytes": must_r,
+                                      "step_gbs": round(must_r / (ms_r * 1e-3) / 1e9, 1)},
+                "device_status": st, "note": "next row N1"}
+
+    attempt(hierarchical)
     attempt(lambda: dict(_decode_line(csa2, dev, "million-token Full decode, B=8, T=1048576, 1% of entries x8", 8,
                                       1 << 20, 3000, 0.01), note="decoder layer"))
     attempt(lambda: dict(_decode_line(csa2, dev, "ratio-2 layer Full decode, B=8, 524288 pooled entries, 1% x8", 8,

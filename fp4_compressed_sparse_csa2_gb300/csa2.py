@@ -23,7 +23,9 @@ KV_PAGE_BYTES, IDX_PAGE_BYTES, IDX_MX_PAGE_BYTES = PAGE * KV_BYTES, PAGE * IDX_B
 IDX_E4M3_16, IDX_MXFP4 = 0, 1  # indexer-K formats (csa2_cache.idx_format)
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_DEVICE = range(7)
-TRACE_KINDS = {"pack": 0, "index": 1, "topk_hist": 2, "topk_select": 3, "topk_final": 4, "attn": 5, "topk": 6}
+TRACE_KINDS = {"pack": 0, "index": 1, "topk_hist": 2, "topk_select": 3, "topk_final": 4, "attn": 5, "topk": 6,
+               "pool": 7, "pool_gather": 8, "pool_map": 9}
+POOL_BLOCK, POOL_BLOCKS, POOL = 8, 2048, 16384  # hierarchical indexer: block, blocks kept, pool positions
 
 
 class Csa2Error(RuntimeError):
@@ -48,7 +50,7 @@ class csa2_step(ctypes.Structure):
                 ("scores", ctypes.c_void_p), ("ld", ctypes.c_int64), ("softmax_scale", ctypes.c_float),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("sinks", ctypes.c_void_p),
                 ("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p), ("win_ring", ctypes.c_void_p),
-                ("win_ring_reqs", ctypes.c_int32)]
+                ("win_ring_reqs", ctypes.c_int32), ("pool", ctypes.c_void_p)]
 
 
 def _load():
@@ -59,6 +61,8 @@ def _load():
     L.csa2_last_error.restype = ctypes.c_char_p
     L.csa2_workspace_bytes.argtypes = [i64, i32, i64, i32]
     L.csa2_workspace_bytes.restype = sz
+    L.csa2_workspace_bytes_pool.argtypes = [i64, i32, i64, i32]
+    L.csa2_workspace_bytes_pool.restype = sz
     L.csa2_pack_kv.argtypes = [vp, vp, vp, vp, i64, ctypes.POINTER(csa2_cache), vp, sz, vp]
     L.csa2_index_score.argtypes = [vp, vp, i32, vp, vp, i64, i32, i64, ctypes.POINTER(csa2_cache), vp, i64, vp,
                                    sz, vp]
@@ -107,12 +111,14 @@ def make_cache(kv: torch.Tensor, idx: torch.Tensor, max_pages: int, block_table:
     return c
 
 
-def workspace_bytes(n_q: int, heads_I: int, t_max: int, scores_in_ws: bool) -> int:
-    return int(lib.csa2_workspace_bytes(int(n_q), int(heads_I), int(t_max), int(bool(scores_in_ws))))
+def workspace_bytes(n_q: int, heads_I: int, t_max: int, scores_in_ws: bool, pool: bool = False) -> int:
+    f = lib.csa2_workspace_bytes_pool if pool else lib.csa2_workspace_bytes
+    return int(f(int(n_q), int(heads_I), int(t_max), int(bool(scores_in_ws))))
 
 
-def alloc_workspace(n_q: int, heads_I: int, t_max: int, scores_in_ws: bool, device="cuda") -> torch.Tensor:
-    n = workspace_bytes(n_q, heads_I, t_max, scores_in_ws)
+def alloc_workspace(n_q: int, heads_I: int, t_max: int, scores_in_ws: bool, device="cuda",
+                    pool: bool = False) -> torch.Tensor:
+    n = workspace_bytes(n_q, heads_I, t_max, scores_in_ws, pool)
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
@@ -150,14 +156,14 @@ def topk_noalloc(scores, ld, n_visible, n_q, t_max, k, out_idx, stream=None):
 def make_step(*, n_q, t_max, q, req, n_visible, window, win_start, win_len, cache, topk_idx, out, q_idx=None,
               w=None, heads_I=64, group=1, n_new=0, new_latent=None, new_idx_key=None, new_req=None, new_pos=None,
               scores=None, ld=0, softmax_scale=0.0, lse=None, sinks=None, rope_cos=None,
-              rope_sin=None, win_ring=None, win_ring_reqs=0) -> csa2_step:
+              rope_sin=None, win_ring=None, win_ring_reqs=0, pool=None) -> csa2_step:
     s = csa2_step(int(n_q), HEADS, int(heads_I), TOPK, int(group), int(t_max), _ptr(q), _ptr(q_idx), _ptr(w),
                   _ptr(req), _ptr(n_visible), _ptr(window), _ptr(win_start), _ptr(win_len), int(n_new),
                   _ptr(new_latent), _ptr(new_idx_key), _ptr(new_req), _ptr(new_pos), cache, _ptr(topk_idx),
                   _ptr(scores), int(ld), float(softmax_scale), _ptr(out), _ptr(lse), _ptr(sinks), _ptr(rope_cos),
-                  _ptr(rope_sin), _ptr(win_ring), int(win_ring_reqs))
+                  _ptr(rope_sin), _ptr(win_ring), int(win_ring_reqs), _ptr(pool))
     s._keep = (q, req, n_visible, window, win_start, win_len, cache, topk_idx, out, q_idx, w, new_latent,
-               new_idx_key, new_req, new_pos, scores, lse, sinks, rope_cos, rope_sin, win_ring)
+               new_idx_key, new_req, new_pos, scores, lse, sinks, rope_cos, rope_sin, win_ring, pool)
     return s
 
 

@@ -52,7 +52,10 @@ csa2_status cuda_fail(cudaError_t e, const char* what) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // ------------------------------------------------------------------ tracing
-enum Kind { kPack = 0, kIndex = 1, kTopkHist = 2, kTopkSel = 3, kTopkFinal = 4, kAttn = 5, kTopk = 6, kKinds = 7 };
+enum Kind {
+  kPack = 0, kIndex = 1, kTopkHist = 2, kTopkSel = 3, kTopkFinal = 4, kAttn = 5, kTopk = 6, kPool = 7, kGather = 8,
+  kMap = 9, kKinds = 10
+};
 constexpr int kTraceCap = 4096;
 
 struct Trace {
@@ -96,20 +99,39 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct WsLayout {
   size_t qpack, scores, topk, total;
   int64_t ld;
+  // candidate pool (hierarchical indexer)
+  size_t bkey, compact, pscores, plen, preq, pslots;
+  int64_t nb_cap;
 };
 
 int64_t ws_ld(int64_t t_max) { return ((t_max + 127) / 128) * 128; }
 
-WsLayout ws_layout(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws) {
-  WsLayout L;
+WsLayout ws_layout(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws, bool pool = false) {
+  WsLayout L{};
   size_t off = kHeader;
+  const size_t nq = static_cast<size_t>(n_q);
   L.qpack = off;
-  off = align256(off + static_cast<size_t>(n_q) * (static_cast<size_t>(heads_I) * 64 + 1024));
+  off = align256(off + nq * (static_cast<size_t>(heads_I) * 64 + 1024));
   L.ld = ws_ld(t_max);
   L.scores = off;
-  if (scores_in_ws) off = align256(off + static_cast<size_t>(n_q) * static_cast<size_t>(L.ld) * 4);
+  if (scores_in_ws) off = align256(off + nq * static_cast<size_t>(L.ld) * 4);
   L.topk = off;
   off = align256(off + topk_ws_bytes(n_q));
+  if (pool) {
+    L.nb_cap = (t_max + CSA2_POOL_BLOCK - 1) / CSA2_POOL_BLOCK;
+    L.bkey = off;
+    off = align256(off + nq * static_cast<size_t>(L.nb_cap) * 4);
+    L.compact = off;  // 128 pages per query, sized for the larger (72-byte) format
+    off = align256(off + nq * (CSA2_POOL / kPage) * static_cast<size_t>(kIdxPageBytes));
+    L.pscores = off;
+    off = align256(off + nq * CSA2_POOL * 4);
+    L.plen = off;
+    off = align256(off + nq * 4);
+    L.preq = off;
+    off = align256(off + nq * 4);
+    L.pslots = off;
+    off = align256(off + nq * CSA2_TOPK * 4);
+  }
   L.total = off;
   return L;
 }
@@ -235,6 +257,67 @@ csa2_status run_topk_cluster(const float* scores, int64_t ld, const int32_t* n_v
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "top-k kernel");
 }
 
+csa2_status run_pool(const float* scores, int64_t ld, const int32_t* n_visible, int64_t n_q, int64_t t_max,
+                     const WsLayout& L, uint8_t* base, int32_t* pool, int32_t* err, cudaStream_t stream) {
+  if (n_q == 0) return CSA2_OK;
+  PoolArgs a{};
+  a.scores = scores;
+  a.ld = ld;
+  a.n_visible = n_visible;
+  a.n_q = n_q;
+  a.bkey = reinterpret_cast<uint32_t*>(base + L.bkey);
+  a.nb_cap = L.nb_cap;
+  a.t_max = L.nb_cap * CSA2_POOL_BLOCK < t_max ? L.nb_cap * CSA2_POOL_BLOCK : t_max;
+  a.pool = pool;
+  a.pool_len = reinterpret_cast<int32_t*>(base + L.plen);
+  a.err = err;
+  trace_begin(kPool, stream);
+  const cudaError_t e = launch_pool(a, stream);
+  trace_end(kPool, stream);
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "pool kernel");
+}
+
+// Reindex over a candidate pool: gather the pool's indexer entries into compact pages,
+// score them with the packed query, take the top-512 of the pool slots, map the slots
+// back to cache positions.
+csa2_status run_pool_reindex(const csa2_step* s, const WsLayout& L, uint8_t* base, int32_t* err,
+                             cudaStream_t stream) {
+  if (s->n_q == 0) return CSA2_OK;
+  GatherArgs g{};
+  g.cache = s->cache;
+  g.pool = s->pool;
+  g.req = s->req;
+  g.n_visible = s->n_visible;
+  g.n_q = s->n_q;
+  g.compact = base + L.compact;
+  g.pool_len = reinterpret_cast<int32_t*>(base + L.plen);
+  g.req_q = reinterpret_cast<int32_t*>(base + L.preq);
+  g.err = err;
+  trace_begin(kGather, stream);
+  cudaError_t e = launch_gather(g, stream);
+  trace_end(kGather, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pool gather kernel");
+  csa2_cache cc{};
+  cc.kv = s->cache.kv;
+  cc.idx = base + L.compact;
+  cc.block_table = nullptr;
+  cc.max_pages = CSA2_POOL / kPage;
+  cc.n_pages = static_cast<int32_t>(s->n_q * (CSA2_POOL / kPage));
+  cc.idx_format = s->cache.idx_format;
+  float* sc = s->scores ? s->scores : reinterpret_cast<float*>(base + L.pscores);
+  const int64_t ld = s->scores ? s->ld : CSA2_POOL;
+  csa2_status st = run_index(cc, base + L.qpack, s->w, s->heads_I, g.req_q, g.pool_len, s->n_q, 1, CSA2_POOL, sc, ld,
+                             err, stream);
+  if (st != CSA2_OK) return st;
+  int32_t* slots = reinterpret_cast<int32_t*>(base + L.pslots);
+  st = run_topk_cluster(sc, ld, g.pool_len, s->n_q, CSA2_POOL, s->topk, slots, err, stream);
+  if (st != CSA2_OK) return st;
+  trace_begin(kMap, stream);
+  e = launch_map(slots, s->pool, s->topk_idx, s->n_q, stream);
+  trace_end(kMap, stream);
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "pool map kernel");
+}
+
 csa2_status run_attn(const csa2_step& s, int32_t* err, cudaStream_t stream) {
   if (s.n_q == 0) return CSA2_OK;
   AttnArgs a{};
@@ -290,8 +373,14 @@ csa2_status check_step(const csa2_step* s, Mode mode) {
     if (s->group != 1 && s->group != 2) return fail(CSA2_ERR_UNSUPPORTED, "group must be 1 or 2");
     if (s->n_q > 0 && (!s->q_idx || !aligned(s->q_idx, 16) || !s->w))
       return fail(CSA2_ERR_INVALID_ARG, "q_idx (16-byte aligned) and w are required");
-    if (s->scores && (s->ld < s->t_max || s->ld % 4 != 0 || !aligned(s->scores, 16)))
-      return fail(CSA2_ERR_INVALID_ARG, "scores needs ld >= t_max, ld %% 4 == 0 and 16-byte alignment");
+    const bool pool_scores = mode == kReindex && s->pool != nullptr;  // scores of the pool slots
+    const int64_t need_ld = pool_scores ? CSA2_POOL : s->t_max;
+    if (s->scores && (s->ld < need_ld || s->ld % 4 != 0 || !aligned(s->scores, 16)))
+      return fail(CSA2_ERR_INVALID_ARG, "scores needs ld >= %s, ld %% 4 == 0 and 16-byte alignment",
+                  pool_scores ? "16384 (pool slots)" : "t_max");
+    if (s->pool != nullptr && !aligned(s->pool, 16))
+      return fail(CSA2_ERR_INVALID_ARG, "pool must be a 16-byte aligned device pointer");
+    if (pool_scores && s->group != 1) return fail(CSA2_ERR_UNSUPPORTED, "a pool-restricted Reindex needs group 1");
   }
   if (mode == kFull && s->n_new > 0) {
     if (!s->new_latent || !s->new_idx_key || !aligned(s->new_latent, 16) || !aligned(s->new_idx_key, 16) ||
@@ -305,10 +394,18 @@ csa2_status run_step(const csa2_step* s, Mode mode, void* ws, size_t ws_bytes, c
   csa2_status st = check_step(s, mode);
   if (st != CSA2_OK) return st;
   const int32_t heads_I = mode == kReuse ? 64 : s->heads_I;
-  const WsLayout L = ws_layout(s->n_q, heads_I, s->t_max, mode != kReuse && s->scores == nullptr);
+  const bool pool = mode != kReuse && s->pool != nullptr;
+  const WsLayout L = ws_layout(s->n_q, heads_I, s->t_max, mode != kReuse && s->scores == nullptr, pool);
   if ((st = check_ws(ws, ws_bytes, L.total)) != CSA2_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(ws);
   int32_t* err = err_word(ws);
+  if (pool && mode == kReindex) {
+    st = run_pack(nullptr, nullptr, nullptr, nullptr, 0, s->cache, s->q_idx, s->n_q, heads_I, 1, base + L.qpack, err,
+                  stream);
+    if (st != CSA2_OK) return st;
+    if ((st = run_pool_reindex(s, L, base, err, stream)) != CSA2_OK) return st;
+    return run_attn(*s, err, stream);
+  }
   if (mode != kReuse) {
     float* scores = s->scores ? s->scores : reinterpret_cast<float*>(base + L.scores);
     const int64_t ld = s->scores ? s->ld : L.ld;
@@ -320,6 +417,10 @@ csa2_status run_step(const csa2_step* s, Mode mode, void* ws, size_t ws_bytes, c
     if (st != CSA2_OK) return st;
     st = run_topk_cluster(scores, ld, s->n_visible, s->n_q, s->t_max, s->topk, s->topk_idx, err, stream);
     if (st != CSA2_OK) return st;
+    if (pool) {  // attention first; the pool serves later layers
+      if ((st = run_attn(*s, err, stream)) != CSA2_OK) return st;
+      return run_pool(scores, ld, s->n_visible, s->n_q, s->t_max, L, base, s->pool, err, stream);
+    }
   }
   return run_attn(*s, err, stream);
 }
@@ -333,6 +434,11 @@ const char* csa2_last_error(void) { return g_last_error.c_str(); }
 size_t csa2_workspace_bytes(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws) {
   if (n_q < 0 || t_max < 0) return 0;
   return ws_layout(n_q, heads_I > 0 ? heads_I : 64, t_max, scores_in_ws).total;
+}
+
+size_t csa2_workspace_bytes_pool(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws) {
+  if (n_q < 0 || t_max < 0) return 0;
+  return ws_layout(n_q, heads_I > 0 ? heads_I : 64, t_max, scores_in_ws, true).total;
 }
 
 csa2_status csa2_pack_kv(const void* latent, const void* idx_key, const int32_t* req, const int64_t* pos, int64_t n,

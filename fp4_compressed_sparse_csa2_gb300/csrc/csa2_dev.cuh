@@ -22,6 +22,7 @@ enum ErrInfo : int32_t {
   kInfoTopkIdx = 3,   // a selected index outside [0, n_visible)
   kInfoGroup = 4,     // queries of one indexer group belong to different requests
   kInfoWait = 5,      // a bounded pipeline wait ran out
+  kInfoPool = 6,      // a candidate pool that is not ascending blocks of 8 visible positions
 };
 
 __device__ __forceinline__ void report(int32_t* err, int32_t status, int32_t info) {

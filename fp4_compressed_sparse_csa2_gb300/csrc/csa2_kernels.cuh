@@ -94,6 +94,31 @@ struct WinPackArgs {
   int32_t* err;
 };
 
+struct PoolArgs {
+  const float* scores;  // [n_q][ld] a Full layer's index scores
+  int64_t ld;
+  const int32_t* n_visible;
+  int64_t n_q;
+  uint32_t* bkey;  // [n_q][nb_cap] scratch: block-maximum keys
+  int64_t nb_cap;  // ceil(t_max / 8)
+  int64_t t_max;   // n_visible[] is clamped to it
+  int32_t* pool;   // [n_q][16384] out: positions ascending, -1 padded
+  int32_t* pool_len;  // [n_q] out
+  int32_t* err;
+};
+
+struct GatherArgs {
+  csa2_cache cache;  // the layer's cache (source pages)
+  const int32_t* pool;  // [n_q][16384]
+  const int32_t* req;
+  const int32_t* n_visible;
+  int64_t n_q;
+  uint8_t* compact;   // [n_q][128 pages] compact indexer pages, same format as the cache
+  int32_t* pool_len;  // [n_q] out: listed positions
+  int32_t* req_q;     // [n_q] out: q (each query owns its compact pages)
+  int32_t* err;
+};
+
 using TraceFn = void (*)(int, cudaStream_t);
 
 // Launches `kernel` so that it may start while the previous kernel on the stream
@@ -139,5 +164,8 @@ cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t st
 size_t attn_smem_bytes();
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_pack_window(const WinPackArgs& a, cudaStream_t stream);
+cudaError_t launch_pool(const PoolArgs& a, cudaStream_t stream);
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_map(const int32_t* slots, const int32_t* pool, int32_t* out, int64_t n_q, cudaStream_t stream);
 
 }  // namespace csa2

@@ -79,7 +79,10 @@ enum {
   CSA2_IDX_PAGE_BYTES = 9216,  /* 128 x 72  */
   CSA2_WIN_BYTES = 528,
   CSA2_IDX_MX_BYTES = 68,        /* MXFP4 indexer key: 64 B of nibbles + 4 E8M0 scales */
-  CSA2_IDX_MX_PAGE_BYTES = 8704  /* 128 x 68 */
+  CSA2_IDX_MX_PAGE_BYTES = 8704, /* 128 x 68 */
+  CSA2_POOL_BLOCK = 8,           /* positions per block of the hierarchical indexer  */
+  CSA2_POOL_BLOCKS = 2048,       /* blocks kept in a candidate pool                  */
+  CSA2_POOL = 16384              /* positions in a full candidate pool (2048 x 8)    */
 };
 
 /* Indexer-K formats (csa2_cache.idx_format).
@@ -179,6 +182,21 @@ typedef struct csa2_step {
    * read; NULL = bf16 window rows as above. */
   const uint8_t* win_ring;   /* optional [win_ring_reqs][128][528]                      */
   int32_t win_ring_reqs;     /* requests in win_ring (bounds check)                    */
+  /* Hierarchical sparse indexer [P1 "The hierarchical indexer"; P4 "The Hierarchical
+   * Sparse Indexer"]: a candidate pool per query, int32 [n_q][16384], the positions of
+   * up to 2,048 blocks of 8 in ascending order, -1 after the last.
+   *   Full mode:    when set, the call also publishes its pool here: every block of 8
+   *                 positions [8j, 8j+8) (visible ones only) gets the maximum of its
+   *                 index scores, the 2,048 largest blocks are kept (equal maxima prefer
+   *                 the lower block, -0 equals +0; all blocks when there are fewer).
+   *   Reindex mode: when set, the call scores only the pool's positions and takes its own
+   *                 top-512 among them (ties to the lower position); `scores`, when
+   *                 given, receives the pool-slot scores [n_q][ld >= 16384], slot i
+   *                 scoring position pool[q][i].  A pool that is not ascending blocks of 8
+   *                 visible positions sets the error word (info 6).  group must be 1.
+   * Either mode needs csa2_workspace_bytes_pool() bytes of workspace; Reuse mode ignores
+ * the pool. */
+  int32_t* pool;
 } csa2_step;
 
 /* Message describing the last failed call on this host thread ("" if none). */
@@ -188,6 +206,12 @@ const char* csa2_last_error(void);
  * entries with heads_I indexer heads; scores_in_ws != 0 when the caller does not
  * provide a score array (the scores then live in the workspace).  Host-only. */
 size_t csa2_workspace_bytes(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws);
+
+/* Workspace bytes for the same calls with a candidate pool (csa2_step.pool set): adds
+ * the block-maximum keys of a Full layer (4 B per 8 entries per query) and, for a
+ * pool-restricted Reindex, the compact indexer pages of each query's pool (128 pages),
+ * its scores and its top-512 slots.  Host-only. */
+size_t csa2_workspace_bytes_pool(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws);
 
 /* Pack n new entries into the cache [P1 "DeepSeek-V4.1", Four bits for the main KV;
  * P3 section 3].  For each 16-channel block: amax = max|x|, scale =
@@ -276,7 +300,8 @@ csa2_status csa2_sparse_attn_reuse(const csa2_step* step, void* ws, size_t ws_by
 
 /* Synchronise `stream`, read and clear the workspace error word.  Returns CSA2_OK,
  * CSA2_ERR_DEVICE or CSA2_ERR_TIMEOUT; *info (may be NULL) receives a code naming the
- * check that failed (1 page id, 2 position, 3 top-k index, 4 group request, 5 wait). */
+ * check that failed (1 page id, 2 position, 3 top-k index, 4 group request, 5 wait,
+ * 6 candidate pool). */
 csa2_status csa2_check(void* ws, csa2_stream_t stream, int32_t* info);
 
 /* Number of kernels this library has launched in this process. */
@@ -286,8 +311,8 @@ int64_t csa2_launch_count(void);
  * csa2_trace_enable(1) starts recording (at most 4096 launches are kept);
  * csa2_trace_read(kind, &ms, &n) synchronises and returns the summed duration and count
  * of kernel `kind` (0 pack/quantise, 1 index score, 2/3/4 histogram, select and final
- * passes of the workspace top-k, 5 attention, 6 cluster top-k); csa2_trace_enable(0)
- * stops and clears. */
+ * passes of the workspace top-k, 5 attention, 6 cluster top-k, 7 candidate pool, 8 pool
+ * gather, 9 pool slot map); csa2_trace_enable(0) stops and clears. */
 csa2_status csa2_trace_enable(int32_t on);
 csa2_status csa2_trace_read(int32_t kind, double* total_ms, int64_t* count);
 
