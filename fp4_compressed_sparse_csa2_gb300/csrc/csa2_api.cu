@@ -54,7 +54,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // ------------------------------------------------------------------ tracing
 enum Kind {
   kPack = 0, kIndex = 1, kTopkHist = 2, kTopkSel = 3, kTopkFinal = 4, kAttn = 5, kTopk = 6, kPool = 7, kGather = 8,
-  kMap = 9, kKinds = 10
+  kMap = 9, kPoolBmax = 10, kKinds = 11
 };
 constexpr int kTraceCap = 4096;
 
@@ -271,8 +271,12 @@ csa2_status run_pool(const float* scores, int64_t ld, const int32_t* n_visible, 
   a.pool = pool;
   a.pool_len = reinterpret_cast<int32_t*>(base + L.plen);
   a.err = err;
+  trace_begin(kPoolBmax, stream);
+  cudaError_t e = launch_pool_bmax(a, stream);
+  trace_end(kPoolBmax, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "block-maximum kernel");
   trace_begin(kPool, stream);
-  const cudaError_t e = launch_pool(a, stream);
+  e = launch_pool(a, stream);
   trace_end(kPool, stream);
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "pool kernel");
 }

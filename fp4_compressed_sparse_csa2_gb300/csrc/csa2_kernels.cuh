@@ -102,6 +102,7 @@ struct PoolArgs {
   uint32_t* bkey;  // [n_q][nb_cap] scratch: block-maximum keys
   int64_t nb_cap;  // ceil(t_max / 8)
   int64_t t_max;   // n_visible[] is clamped to it
+  int32_t stage;   // set by the launcher: dynamic shared memory holds min(nb_cap, 32768) keys
   int32_t* pool;   // [n_q][16384] out: positions ascending, -1 padded
   int32_t* pool_len;  // [n_q] out
   int32_t* err;
@@ -164,7 +165,8 @@ cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t st
 size_t attn_smem_bytes();
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_pack_window(const WinPackArgs& a, cudaStream_t stream);
-cudaError_t launch_pool(const PoolArgs& a, cudaStream_t stream);
+cudaError_t launch_pool_bmax(const PoolArgs& a, cudaStream_t stream);  // block maxima (first)
+cudaError_t launch_pool(const PoolArgs& a, cudaStream_t stream);       // the selection
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_map(const int32_t* slots, const int32_t* pool, int32_t* out, int64_t n_q, cudaStream_t stream);
 

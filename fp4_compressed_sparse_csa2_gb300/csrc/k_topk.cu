@@ -815,8 +815,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
   const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
   // Long rows go by 32-entry block maxima: the k-th largest block maximum bounds the
   // k-th largest key from below (k blocks each hold a key at least that large), so only
-  // blocks reaching the bound are read again.  Short rows histogram every key.
-  const bool by_blocks = (nv + 31) / 32 >= a.k && chunk / 32 <= kClBlockCap;  // uniform across the cluster
+  // blocks reaching the bound are read again.  That pays when the row has many more
+  // blocks than k (with about k blocks the bound is the smallest block maximum and every
+  // block is read again); shorter rows histogram every key.
+  const bool by_blocks = (nv + 31) / 32 >= 4 * a.k && chunk / 32 <= kClBlockCap;  // uniform across the cluster
   for (int b = threadIdx.x; b < 2 * kBins; b += kTopkThreads) h[b] = 0;
   if (threadIdx.x < 8) ctr[threadIdx.x] = 0;  // ctr and lctr
   __syncthreads();

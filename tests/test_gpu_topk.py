@@ -76,6 +76,6 @@ def test_topk_increasing_rows_overflow_to_whole_row(orc, csa2):
     # increasing scores make the block bound as loose as it gets (every entry of the last
     # 512 blocks is a candidate): the staged lists overflow and the leader selects over
     # the whole row; exact ties across blocks ride along
-    t = 60000
+    t = 70000
     S = np.stack([np.arange(t, dtype=np.float32), np.repeat(np.arange(t // 40, dtype=np.float32), 40)[:t]])
     _check(orc, csa2, S, [t, t])
