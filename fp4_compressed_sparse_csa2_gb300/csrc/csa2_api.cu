@@ -4,6 +4,7 @@
 // mode orchestration (Full = pack + index + top-k + attention; Reindex = index +
 // top-k + attention on a shared cache; Reuse = attention on given indices), a launch
 // counter and optional per-kernel CUDA-event timing.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -54,7 +55,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // ------------------------------------------------------------------ tracing
 enum Kind {
   kPack = 0, kIndex = 1, kTopkHist = 2, kTopkSel = 3, kTopkFinal = 4, kAttn = 5, kTopk = 6, kPool = 7, kGather = 8,
-  kMap = 9, kPoolBmax = 10, kKinds = 11
+  kMap = 9, kPoolBmax = 10, kAttnCombine = 11, kKinds = 12
 };
 constexpr int kTraceCap = 4096;
 
@@ -97,7 +98,7 @@ constexpr size_t kHeader = 256;
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t qpack, scores, topk, total;
+  size_t qpack, scores, topk, apart, total;
   int64_t ld;
   // candidate pool (hierarchical indexer)
   size_t bkey, compact, pscores, plen, preq, pslots;
@@ -117,6 +118,8 @@ WsLayout ws_layout(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_i
   if (scores_in_ws) off = align256(off + nq * static_cast<size_t>(L.ld) * 4);
   L.topk = off;
   off = align256(off + topk_ws_bytes(n_q));
+  L.apart = off;  // partial outputs of the attention's key-tile splits (small batches)
+  off = align256(off + attn_split_ws_bytes(n_q));
   if (pool) {
     L.nb_cap = (t_max + CSA2_POOL_BLOCK - 1) / CSA2_POOL_BLOCK;
     L.bkey = off;
@@ -322,7 +325,7 @@ csa2_status run_pool_reindex(const csa2_step* s, const WsLayout& L, uint8_t* bas
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "pool map kernel");
 }
 
-csa2_status run_attn(const csa2_step& s, int32_t* err, cudaStream_t stream) {
+csa2_status run_attn(const csa2_step& s, uint8_t* base, const WsLayout& L, int32_t* err, cudaStream_t stream) {
   if (s.n_q == 0) return CSA2_OK;
   AttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(s.q);
@@ -344,10 +347,26 @@ csa2_status run_attn(const csa2_step& s, int32_t* err, cudaStream_t stream) {
   a.rope_sin = s.rope_sin;
   a.win_ring = s.win_ring;
   a.win_ring_reqs = s.win_ring_reqs;
+  // small batches split each query's key tiles over several CTAs (plain path only); the
+  // workspace holds the partials for the split count of a 304-SM part at most
+  const bool ext = s.sinks != nullptr || s.rope_cos != nullptr || s.win_ring != nullptr;
+  const int S = std::min(attn_splits(s.n_q, sm_count()), attn_splits(s.n_q, 304));
+  a.splits = ext ? 1 : S;
+  if (a.splits > 1) {
+    a.opart = reinterpret_cast<float*>(base + L.apart);
+    a.lpart = a.opart + static_cast<size_t>(s.n_q) * a.splits * CSA2_HEADS * CSA2_D;
+  }
   trace_begin(kAttn, stream);
-  const cudaError_t e = launch_attn(a, stream);
+  cudaError_t e = launch_attn(a, stream);
   trace_end(kAttn, stream);
-  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "attention kernel");
+  if (e != cudaSuccess) return cuda_fail(e, "attention kernel");
+  if (a.splits > 1) {
+    trace_begin(kAttnCombine, stream);
+    e = launch_attn_combine(a, stream);
+    trace_end(kAttnCombine, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attention combine kernel");
+  }
+  return CSA2_OK;
 }
 
 enum Mode { kFull, kReindex, kReuse };
@@ -408,7 +427,7 @@ csa2_status run_step(const csa2_step* s, Mode mode, void* ws, size_t ws_bytes, c
                   stream);
     if (st != CSA2_OK) return st;
     if ((st = run_pool_reindex(s, L, base, err, stream)) != CSA2_OK) return st;
-    return run_attn(*s, err, stream);
+    return run_attn(*s, base, L, err, stream);
   }
   if (mode != kReuse) {
     float* scores = s->scores ? s->scores : reinterpret_cast<float*>(base + L.scores);
@@ -422,11 +441,11 @@ csa2_status run_step(const csa2_step* s, Mode mode, void* ws, size_t ws_bytes, c
     st = run_topk_cluster(scores, ld, s->n_visible, s->n_q, s->t_max, s->topk, s->topk_idx, err, stream);
     if (st != CSA2_OK) return st;
     if (pool) {  // attention first; the pool serves later layers
-      if ((st = run_attn(*s, err, stream)) != CSA2_OK) return st;
+      if ((st = run_attn(*s, base, L, err, stream)) != CSA2_OK) return st;
       return run_pool(scores, ld, s->n_visible, s->n_q, s->t_max, L, base, s->pool, err, stream);
     }
   }
-  return run_attn(*s, err, stream);
+  return run_attn(*s, base, L, err, stream);
 }
 
 }  // namespace

@@ -82,7 +82,27 @@ struct AttnArgs {
   const float* rope_sin;
   const uint8_t* win_ring;  // FP8 window ring [win_ring_reqs][128][528] or nullptr
   int32_t win_ring_reqs;
+  // split over the key tiles (plain path only): splits CTAs per (query, head half), each
+  // over a run of the tile list [window, selected 0..3]; they write normalised fp32
+  // partial outputs and log2 sum-exps that attn_combine_kernel merges
+  int32_t splits;  // 1 = no split (the output is written directly)
+  float* opart;    // [n_q][splits][64][512]
+  float* lpart;    // [n_q][splits][64]
 };
+
+// Key-tile splits per (query, head half) for n_q queries on sm_count SMs: the most (up to
+// the 5 tiles) that keep all CTAs in one wave; 1 when two CTAs per query already fill it.
+constexpr int kAttnMaxSplits = 5;
+inline int attn_splits(int64_t n_q, int sm_count) {
+  if (n_q <= 0) return 1;
+  const int64_t s = sm_count / (2 * n_q);
+  return static_cast<int>(s < 1 ? 1 : (s > kAttnMaxSplits ? kAttnMaxSplits : s));
+}
+// Workspace bytes for the partial outputs of n_q queries (sized for up to 304 SMs).
+inline size_t attn_split_ws_bytes(int64_t n_q) {
+  const int s = attn_splits(n_q, 304);
+  return s > 1 ? static_cast<size_t>(n_q) * s * 64 * (512 + 1) * sizeof(float) : 0;
+}
 
 struct WinPackArgs {
   const __nv_bfloat16* rows;  // [n][512]
@@ -163,7 +183,8 @@ cudaError_t smem_limit_once(const void* kernel, size_t bytes, std::atomic<int>* 
 cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes);
 cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream);
 size_t attn_smem_bytes();
-cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);          // a.splits > 1: then the combine
+cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream);  // merges the key-tile splits
 cudaError_t launch_pack_window(const WinPackArgs& a, cudaStream_t stream);
 cudaError_t launch_pool_bmax(const PoolArgs& a, cudaStream_t stream);  // block maxima (first)
 cudaError_t launch_pool(const PoolArgs& a, cudaStream_t stream);       // the selection

@@ -77,8 +77,9 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_newest_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // kExt: the optional features (sinks, partial RoPE, FP8 window ring) are compiled in;
-// the plain instance carries none of their code.
-template <bool kExt>
+// the plain instance carries none of their code.  kSplit (plain path only): a.splits CTAs
+// per (query, head half) each take a run of the key tiles and write a partial.
+template <bool kExt, bool kSplit>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -98,8 +99,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   int32_t* flags = reinterpret_cast<int32_t*>(tmem_slot + 1);  // [0] abort, [1] rescale
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t qi = blockIdx.x >> 1;
+  const int S = kSplit ? a.splits : 1;  // CTAs per (query, head half), each over a run of tiles
+  const int64_t qi = blockIdx.x / (2 * S);
+  const int sp = static_cast<int>((blockIdx.x >> 1) % S);
   const int h0 = (blockIdx.x & 1) * kHH;  // first head of this CTA
+  // this CTA's run [t_lo, t_hi) of the tile list [window, selected 0, 1, 2, 3]
+  const int t_lo = sp * 5 / S, t_hi = (sp + 1) * 5 / S;
+  const bool has_win = t_lo == 0;
+  const int sel_lo = t_lo == 0 ? 0 : t_lo - 1, sel_hi = t_hi - 1;  // selected tiles [sel_lo, sel_hi)
   const int32_t nv = __ldg(a.n_visible + qi);
   const int32_t wl = max(0, min(CSA2_WIN, __ldg(a.win_len + qi)));
 
@@ -129,7 +136,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     }
     cp_async_commit();
     const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
-    const bool bf16_rows = !kExt || a.win_ring == nullptr;
+    const bool bf16_rows = (!kExt || a.win_ring == nullptr) && has_win;
     for (int c = tid; bf16_rows && c < 128 * 64; c += kAttnThreads) {  // bf16 window rows
       uint32_t r, ch;
       tile_item(static_cast<uint32_t>(c), 128, r, ch);
@@ -179,12 +186,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     }
     cp_async_commit();
   };
-  auto next_selected = [&](int t) {  // first selected tile after t with any entry, or 4
+  auto next_selected = [&](int t) {  // first selected tile of this run after t with any entry, or 4
     int u = t + 1;
-    while (u < 4 && tile_cnt[u] == 0) ++u;
-    return u;
+    while (u < sel_hi && tile_cnt[u] == 0) ++u;
+    return u < sel_hi ? u : 4;
   };
-  int staged = next_selected(-1);
+  int staged = next_selected(sel_lo - 1);
   if (staged < 4) prefetch(staged);
 
   float lsum[16];
@@ -198,8 +205,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
 
   for (int it = 0; it < 5; ++it) {
     // ---------------------------------------------------------------- the key tile
-    const int t = it == 0 ? 4 : staged;  // the window first, then the selected tiles in order
-    if (t == 4 && it > 0) break;         // no selected tile left
+    const bool win_turn = it == 0 && has_win;
+    const int t = win_turn ? 4 : staged;  // the window first, then the selected tiles in order
+    if (t == 4 && !win_turn) break;       // no selected tile left
     if (t == 4) {
       if (staged < 4) cp_async_wait_newest_pending();  // queries and window landed; records may still fly
       else cp_async_wait_all();
@@ -422,7 +430,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     if (tid < kHH) {
       const float l = lred[tid] + lred[kHH + tid] + lred[2 * kHH + tid] + lred[3 * kHH + tid];
       float lse2 = -INFINITY, inv = 0.0f;  // log2 sum-exp; O = O^T * inv
-      if (!kExt || a.sinks == nullptr) {
+      if (kSplit) {  // a partial over this CTA's tiles, merged by attn_combine_kernel
+        if (l > 0.0f) {
+          lse2 = ref[tid] + log2f(l);
+          inv = 1.0f / l;
+        }
+        a.lpart[(qi * S + sp) * kHeads + h0 + tid] = lse2;
+      } else if (!kExt || a.sinks == nullptr) {
         if (l > 0.0f) {
           lse2 = ref[tid] + log2f(l);
           inv = 1.0f / l;
@@ -438,7 +452,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
           inv = l > 0.0f ? exp2f(ref[tid] - m2) / lt : 0.0f;
         }
       }
-      if (a.lse) a.lse[qi * kHeads + h0 + tid] = lse2 * 0.6931471805599453f;
+      if (a.lse && !kSplit) a.lse[qi * kHeads + h0 + tid] = lse2 * 0.6931471805599453f;
       alpha[tid] = inv;  // reuse: the output scale per head
     }
     __syncthreads();
@@ -447,7 +461,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(Kt);
     float* otail = reinterpret_cast<float*>(Ps);  // [32 heads][64] fp32 rotated channels (RoPE)
     const bool rope = kExt && a.rope_cos != nullptr;
-    for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
+    if (kSplit) {
+      // the normalised partial in fp32 [32][512], staged in the free key tile, then 16-byte
+      // coalesced stores
+      float* fstage = reinterpret_cast<float*>(Kt);
+      for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
+        const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
+        uint32_t r[32];
+        if (o_started) {
+          tmem_ld32(tmem + lane_base + kOCols + static_cast<uint32_t>(c * kHH), r);
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) fstage[i * CSA2_D + d] = o_started ? __uint_as_float(r[i]) * alpha[i] : 0.0f;
+      }
+      __syncthreads();
+      uint4* pg = reinterpret_cast<uint4*>(a.opart + ((qi * S + sp) * kHeads + h0) * CSA2_D);
+      const uint4* fs = reinterpret_cast<const uint4*>(fstage);
+      for (int i = tid; i < kHH * CSA2_D / 4; i += kAttnThreads) pg[i] = fs[i];
+    }
+    for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2 && !kSplit; ++c) {
       const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
       uint32_t r[32];
       if (o_started) {
@@ -480,7 +513,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     __syncthreads();
     uint4* og = reinterpret_cast<uint4*>(a.out + (qi * kHeads + h0) * CSA2_D);
     const uint4* os = reinterpret_cast<const uint4*>(ostage);
-    for (int i = tid; i < kHH * CSA2_D / 8; i += kAttnThreads) og[i] = os[i];
+    for (int i = tid; i < kHH * CSA2_D / 8 && !kSplit; i += kAttnThreads) og[i] = os[i];
   }
   // drain outstanding MMAs, then free TMEM
   if (lane == 0 && warp < 2) {
@@ -498,15 +531,75 @@ size_t attn_smem_bytes() {
          4 * sizeof(uint64_t) + 16;
 }
 
+// Merge of the key-tile splits: one warp per (query, head).  The total log2 sum-exp is
+// L = log2(sum_s 2^L_s) and O = sum_s 2^(L_s - L) O_s (each O_s already normalised by
+// its own sum); lanes take 16 channels each.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();  // the partials come from the attention kernel
+  const int lane = threadIdx.x & 31;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (item >= a.n_q * kHeads) return;
+  const int64_t qi = item / kHeads;
+  const int h = static_cast<int>(item % kHeads);
+  const int S = a.splits;
+  float ls[kAttnMaxSplits];
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kAttnMaxSplits; ++s) {
+    ls[s] = s < S ? __ldg(a.lpart + (qi * S + s) * kHeads + h) : -INFINITY;
+    m = fmaxf(m, ls[s]);
+  }
+  float tot = 0.0f;
+#pragma unroll
+  for (int s = 0; s < kAttnMaxSplits; ++s) tot += ls[s] == -INFINITY ? 0.0f : exp2f(ls[s] - m);
+  const float lse2 = m == -INFINITY ? -INFINITY : m + log2f(tot);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < kAttnMaxSplits; ++s) {
+    if (ls[s] == -INFINITY) continue;
+    const float wgt = exp2f(ls[s] - lse2);
+    const float4* src = reinterpret_cast<const float4*>(a.opart + ((qi * S + s) * kHeads + h) * CSA2_D + 16 * lane);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = __ldg(src + k);
+      acc[4 * k + 0] += wgt * v.x;
+      acc[4 * k + 1] += wgt * v.y;
+      acc[4 * k + 2] += wgt * v.z;
+      acc[4 * k + 3] += wgt * v.w;
+    }
+  }
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    o[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.out + (qi * kHeads + h) * CSA2_D + 16 * lane);
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  if (lane == 0 && a.lse) a.lse[qi * kHeads + h] = lse2 * 0.6931471805599453f;
+}
+
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_q == 0) return cudaSuccess;
   const size_t smem = attn_smem_bytes();
-  static std::atomic<int> limit_set[2][kMaxDevices];
+  static std::atomic<int> limit_set[3][kMaxDevices];
   const bool ext = a.sinks != nullptr || a.rope_cos != nullptr || a.win_ring != nullptr;
-  auto* kernel = ext ? attn_kernel<true> : attn_kernel<false>;
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kernel), smem, limit_set[ext ? 1 : 0]);
+  const int S = ext ? 1 : a.splits;
+  auto* kernel = ext ? attn_kernel<true, false> : (S > 1 ? attn_kernel<false, true> : attn_kernel<false, false>);
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kernel), smem, limit_set[ext ? 2 : (S > 1 ? 1 : 0)]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kernel, dim3(static_cast<unsigned>(2 * a.n_q)), dim3(kAttnThreads), smem, stream, nullptr, a);
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(2 * a.n_q * S)), dim3(kAttnThreads), smem, stream, nullptr,
+                    a);
+}
+
+cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream) {
+  if (a.n_q == 0) return cudaSuccess;
+  const int64_t blocks = (a.n_q * kHeads + 7) / 8;
+  return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, nullptr, a);
 }
 
 }  // namespace csa2

@@ -134,3 +134,33 @@ def test_attn_bounded_replay_window(orc, csa2):
     assert lens == [1, 2, 61, 128, 128, 128]
     idx = np.stack([synth.distinct_indices(30 + i, 1000, 512) for i in range(len(pos))])
     _reuse(orc, csa2, n, idx, [0] * len(pos), lens, seed=57, win_rows=301 + base, win_start=starts)
+
+
+@pytest.mark.parametrize("n_q", [17, 22, 30])
+def test_attn_key_tile_splits(orc, csa2, n_q):
+    """Small batches split each query's key tiles over several CTAs and merge the partial
+    outputs by their sums of exponentials; on 152 SMs these batch sizes take 4, 3 and 2
+    splits (smaller batches take 5).  Rows mix full selections, short selections (empty
+    tiles in some splits), window-only rows and rows with no key at all."""
+    n = [700, 300]
+    pats = []
+    for i in range(n_q):
+        k = i % 5
+        if k == 0:
+            pats.append(synth.distinct_indices(60 + i, 700, 512))
+        elif k == 1:
+            pats.append(synth.distinct_indices(60 + i, 300, 512))      # 300 valid, then -1
+        elif k == 2:
+            pats.append(np.full(512, -1, np.int32))                    # window only
+        elif k == 3:
+            a = np.full(512, -1, np.int32)
+            a[:3] = [0, 299, 150]
+            pats.append(a)
+        else:
+            a = synth.distinct_indices(60 + i, 700, 512)
+            a[300:] = -1                                               # the last two tiles empty
+            pats.append(a)
+    req = [0 if i % 5 in (0, 4) else 1 for i in range(n_q)]
+    win = [[128, 57, 0, 128, 1][i % 5] if i % 7 else 0 for i in range(n_q)]
+    win[2] = 0                                                         # a row with no key at all
+    _reuse(orc, csa2, n, np.stack(pats), req, win, seed=58 + n_q)
