@@ -64,7 +64,8 @@ def _reuse(orc, csa2, n_entries, idx, req_q, win_len, seed, qscale=1.0, win_rows
         assert err <= TOL, (i, err)
         fin = np.isfinite(lref)
         assert np.array_equal(fin, np.isfinite(L[i]))
-        assert np.abs(L[i][fin] - lref[fin]).max() <= 1e-2
+        if fin.any():  # a query with no key at all has lse = -inf in every head
+            assert np.abs(L[i][fin] - lref[fin]).max() <= 1e-2
     return O
 
 
