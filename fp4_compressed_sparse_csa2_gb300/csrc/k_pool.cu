@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kBmaxThreads) bmax_kernel(const PoolArgs a) {
 }
 
 constexpr int64_t kPoolStage = 32768;  // block keys staged in shared memory (128 KB)
+constexpr uint32_t kPoolList = 2048;    // keys still in play kept for the last radix level
 constexpr int kKeyUnroll = 8;          // independent key loads in flight per thread
 
 // f(j, key) for every j < nb, each thread 8 keys a round with all loads issued first.
@@ -154,7 +155,8 @@ __global__ void __launch_bounds__(kPoolThreads, 1) pool_kernel(const PoolArgs a)
   __shared__ uint32_t h[2048];
   __shared__ uint32_t s_scan[33];
   __shared__ uint32_t s_gt[kPoolWarps], s_tie[kPoolWarps], s_tbase[kPoolWarps], s_sbase[kPoolWarps];
-  __shared__ uint32_t s_bin, s_above, s_last;
+  __shared__ uint32_t s_bin, s_above, s_lcnt;
+  __shared__ uint32_t s_list[kPoolList];  // keys in play (radix levels), then the kept block ids
   pdl_trigger();
   pdl_wait();  // the scores come from the previous kernel
   const int64_t q = blockIdx.x;
@@ -194,20 +196,40 @@ __global__ void __launch_bounds__(kPoolThreads, 1) pool_kernel(const PoolArgs a)
   const uint32_t K = CSA2_POOL_BLOCKS;
   const uint32_t span = hi - lo;
   uint32_t m_shift = span ? 32u - static_cast<uint32_t>(__clz(span)) : 0u, m_val = 0u, above = 0u;
+  // a level whose keys in play fit the list copies them there on its pass over the row,
+  // so the levels after it scan only the list
+  uint32_t in_play = static_cast<uint32_t>(nb), list_n = 0;
+  bool from_list = false;
   while (m_shift > 0u) {
     const uint32_t c_shift = m_shift > 11u ? m_shift - 11u : 0u;
     const uint32_t width = m_shift - c_shift;
+    const bool collect = !from_list && c_shift > 0u && in_play <= kPoolList;
     for (int b = threadIdx.x; b < 2048; b += kPoolThreads) h[b] = 0u;
+    if (threadIdx.x == 0) s_lcnt = 0u;
     __syncthreads();
-    for_keys(key, nb, [&](int64_t, uint32_t k) {
+    auto visit = [&](uint32_t k) {
       const uint32_t d = k - lo;
-      if ((static_cast<uint64_t>(d) >> m_shift) == m_val) atomicAdd(&h[(d >> c_shift) & ((1u << width) - 1u)], 1u);
-    });
+      if ((static_cast<uint64_t>(d) >> m_shift) == m_val) {
+        atomicAdd(&h[(d >> c_shift) & ((1u << width) - 1u)], 1u);
+        if (collect) s_list[atomicAdd(&s_lcnt, 1u)] = k;  // at most in_play <= kPoolList keys
+      }
+    };
+    if (from_list) {
+      for (uint32_t i = threadIdx.x; i < list_n; i += kPoolThreads) visit(s_list[i]);
+    } else {
+      for_keys(key, nb, [&](int64_t, uint32_t k) { visit(k); });
+    }
     __syncthreads();
     pool_threshold(h, 1 << width, K - above, s_scan, &s_bin, &s_above);
+    in_play = h[s_bin];
+    if (collect) {
+      from_list = true;
+      list_n = s_lcnt;
+    }
     m_val = (m_val << width) | s_bin;
     above += s_above;
     m_shift = c_shift;
+    __syncthreads();  // h, s_bin and s_lcnt are read above before the next level resets them
   }
   const uint32_t vstar = lo + m_val;
   const uint32_t need = K - above;  // blocks equal to v* to keep, lowest index first
@@ -232,7 +254,6 @@ __global__ void __launch_bounds__(kPoolThreads, 1) pool_kernel(const PoolArgs a)
     s_gt[warp] = gt;
     s_tie[warp] = tie;
   }
-  if (threadIdx.x == 0) s_last = 0u;
   __syncthreads();
   if (warp == 0) {
     const uint32_t t = s_tie[lane];
@@ -265,23 +286,21 @@ __global__ void __launch_bounds__(kPoolThreads, 1) pool_kernel(const PoolArgs a)
     const uint32_t smask = __ballot_sync(0xffffffffu, sel);
     if (sel) {
       const uint32_t slot = sr + __popc(smask & lt);
-      if (slot < K) {
-        int32_t v[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = 8 * j + t < nv ? static_cast<int32_t>(8 * j + t) : -1;
-        int4* dst = reinterpret_cast<int4*>(out + 8 * static_cast<int64_t>(slot));
-        dst[0] = make_int4(v[0], v[1], v[2], v[3]);
-        dst[1] = make_int4(v[4], v[5], v[6], v[7]);
-        if (j == nb - 1) s_last = 1u;
-      }
+      if (slot < K) s_list[slot] = static_cast<uint32_t>(j);  // kept blocks in ascending order
     }
     tr += __popc(tmask);
     sr += __popc(smask);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  // positions of the kept blocks, ascending: plain coalesced stores
+  for (int i = threadIdx.x; i < CSA2_POOL; i += kPoolThreads) {
+    const int64_t p = 8 * static_cast<int64_t>(s_list[i >> 3]) + (i & 7);
+    out[i] = p < nv ? static_cast<int32_t>(p) : -1;
+  }
+  if (threadIdx.x == 0) {  // only the last block can be partial, and it is kept last
     const int64_t part = nv % CSA2_POOL_BLOCK;
-    a.pool_len[q] = static_cast<int32_t>(CSA2_POOL - (s_last && part ? CSA2_POOL_BLOCK - part : 0));
+    const bool last = s_list[K - 1] == static_cast<uint32_t>(nb - 1);
+    a.pool_len[q] = static_cast<int32_t>(CSA2_POOL - (last && part ? CSA2_POOL_BLOCK - part : 0));
   }
 }
 
