@@ -150,6 +150,13 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workload
+def rank_seed_base(rank: int) -> int:
+    """Seed base of a rank's replica batch: per-request seed = 1000*config + request, plus
+    100,000 per rank (latent seeds base + r, key seeds base + r + 50,000, step inputs
+    base + 7,000,000 + i), so the ranks' requests never share a seed."""
+    return 1000 * 1 + 100000 * rank
+
+
 class Workload:
     """Seeded synthetic Full-mode decode step resident on the device."""
 
@@ -164,7 +171,7 @@ class Workload:
         self.idx = torch.empty(n_pages * csa2.IDX_PAGE_BYTES, dtype=torch.uint8, device=device)
         self.cache = csa2.make_cache(self.kv, self.idx, self.max_pages)
         ws0 = csa2.alloc_workspace(1, 64, 0, False, device)
-        base = 1000 * 1 + 100000 * rank          # per-request seed = 1000*config + request (+ rank offset)
+        base = rank_seed_base(rank)
         pos = torch.arange(T - 1, dtype=torch.int64, device=device)
         for r in range(B):
             lat = synth.torch_normal_bf16(base + r, (T - 1, D), device)
