@@ -19,20 +19,20 @@ from helpers import Cache, dev, dev_bf16, fill_cache
 pytestmark = pytest.mark.gpu
 
 
-def _setup(orc, csa2, B, T, seed, mx):
+def _setup(orc, csa2, B, T, seed, mx, block_table=None):
     max_pages = (T + 127) // 128
-    cache = Cache(B, max_pages, mx=mx)
+    cache = Cache(B, max_pages, mx=mx, block_table=block_table)
+    bt = cache.bt_np
     lat, key, req_e, pos_e = fill_cache(cache, [T] * B, seed)
     if mx:
-        kv_h = None
         ix_h = orc.alloc_idx_mx_pages(cache.n_pages)
-        orc.pack_idx_mx(key, req_e, pos_e, ix_h, None, max_pages)
+        orc.pack_idx_mx(key, req_e, pos_e, ix_h, bt, max_pages)
         kv_h, _ = orc.alloc_pages(cache.n_pages)
-        orc.pack_kv(lat, key, req_e, pos_e, kv_h, np.zeros(cache.n_pages * orc.IDX_PAGE_BYTES, np.uint8), None,
+        orc.pack_kv(lat, key, req_e, pos_e, kv_h, np.zeros(cache.n_pages * orc.IDX_PAGE_BYTES, np.uint8), bt,
                     max_pages)
     else:
         kv_h, ix_h = orc.alloc_pages(cache.n_pages)
-        orc.pack_kv(lat, key, req_e, pos_e, kv_h, ix_h, None, max_pages)
+        orc.pack_kv(lat, key, req_e, pos_e, kv_h, ix_h, bt, max_pages)
     window = synth.normal_bf16(seed + 16, (B * 128, 512))
     common = dict(n_q=B, t_max=T, req=dev(np.arange(B, dtype=np.int32)), n_visible=dev(np.full(B, T, np.int32)),
                   window=dev_bf16(window), win_start=dev(np.arange(B, dtype=np.int64) * 128),
@@ -121,3 +121,39 @@ def test_pool_scores_in_workspace_and_malformed_pool(orc, csa2):
     c["ld"] = 0
     csa2.sparse_attn_reindex(csa2.make_step(**common, q=q, q_idx=qi, w=w, pool=bad, **c), ws)
     assert csa2.check(ws) == (csa2.ERR_DEVICE, 6)
+
+
+@pytest.mark.parametrize("mx", [False, True])
+def test_pool_over_a_block_table(orc, csa2, mx):
+    """Paged cache with a permuted block table: the gather resolves every pooled block's
+    page through it."""
+    B, T = 2, 24000
+    mp = (T + 127) // 128
+    perm = np.random.default_rng(960 + mx).permutation(B * mp).astype(np.int32).reshape(B, mp)
+    cache, kv_h, ix_h, window, mp, common = _setup(orc, csa2, B, T, 961, mx, block_table=perm)
+    bt = cache.bt_np
+    q = synth.normal_bf16(962, (B, 64, 512))
+    qi = synth.normal_bf16(963, (B, 64, 128))
+    w = synth.normal_f32(964, (B, 64))
+    ws = csa2.alloc_workspace(B, 64, T, False, pool=True)
+    pool = torch.full((B, 16384), -7, dtype=torch.int32, device="cuda")
+    full = _outs(B, ((T + 3) // 4) * 4)
+    csa2.sparse_attn_full(csa2.make_step(**common, q=dev_bf16(q), q_idx=dev_bf16(qi), w=dev(w), pool=pool, **full),
+                          ws)
+    qi2 = synth.normal_bf16(965, (B, 64, 128))
+    w2 = synth.normal_f32(966, (B, 64))
+    re = _outs(B, 16384)
+    csa2.sparse_attn_reindex(csa2.make_step(**common, q=dev_bf16(q), q_idx=dev_bf16(qi2), w=dev(w2), pool=pool,
+                                            **re), ws)
+    assert csa2.check(ws) == (csa2.OK, 0)
+    S, P = full["scores"].cpu().numpy(), pool.cpu().numpy()
+    G, idx = re["scores"].cpu().numpy(), re["topk_idx"].cpu().numpy()
+    O = re["out"].float().cpu().numpy()
+    for b in range(B):
+        ref, n = orc.block_pool(S[b, :T], T)
+        assert np.array_equal(P[b], ref)
+        I, M = orc.index_score_at(qi2[b], w2[b], ix_h, b, P[b, :n], mx=mx, block_table=bt, max_pages=mp)
+        assert (np.abs(G[b, :n] - I) <= 1e-3 * M).all()
+        assert np.array_equal(idx[b], orc.pool_topk(G[b, :n], P[b], n, 512))
+        Oref, _ = orc.attention(q[b], idx[b], kv_h, b, window[128 * b:128 * b + 128], 128, None, bt, mp)
+        assert np.abs(O[b] - Oref).max() <= 2e-2
