@@ -114,10 +114,11 @@ def _declare(L):
     L.or_block_pool.restype = ctypes.c_int64
     L.or_index_score_at.argtypes = [_u16p, _f32p, ctypes.c_int32, _u8p, _i32p, ctypes.c_int32, ctypes.c_int32,
                                     _i32p, ctypes.c_int64, ctypes.c_int32, _f64p, _f64p]
+    L.or_index_score_bf16.argtypes = [_u16p, _f32p, ctypes.c_int32, _u16p, ctypes.c_int64, _f64p]
     for f in ("or_quant_block16", "or_quant_vector", "or_pack_kv", "or_read_main", "or_read_idx",
               "or_index_score", "or_topk", "or_attention", "or_attention_ext", "or_pack_window",
               "or_read_window", "or_attention_ring", "or_mx_quant_block32", "or_pack_idx_mx",
-              "or_read_idx_mx", "or_index_score_mx", "or_index_score_at"):
+              "or_read_idx_mx", "or_index_score_mx", "or_index_score_at", "or_index_score_bf16"):
         getattr(L, f).restype = None
 
 
@@ -474,3 +475,15 @@ def pool_topk(pool_scores, pool, n: int, k: int = 512) -> np.ndarray:
     returned as positions ascending, -1 padded [P4 "The Hierarchical Sparse Indexer"]."""
     slots = topk(np.ascontiguousarray(pool_scores, dtype=np.float32)[:n], k)
     return np.where(slots >= 0, np.asarray(pool)[np.maximum(slots, 0)], -1).astype(np.int32)
+
+
+def index_score_bf16(q_idx_bf16, w, keys_bf16) -> np.ndarray:
+    """The index score from the unquantised bf16 query and keys (fp64): the reference for
+    the recall of the FP4 selection [P1 "DeepSeek-V4", 99.7 % recall quoted for V4]."""
+    q = np.ascontiguousarray(q_idx_bf16, dtype=np.uint16)
+    k = np.ascontiguousarray(keys_bf16, dtype=np.uint16)
+    heads = q.shape[0]
+    wf = np.ascontiguousarray(w, dtype=np.float32)
+    I = np.zeros(k.shape[0], np.float64)
+    lib().or_index_score_bf16(_p(q, _u16p), _p(wf, _f32p), heads, _p(k, _u16p), k.shape[0], _p(I, _f64p))
+    return I

@@ -650,3 +650,24 @@ void or_index_score_at(const uint16_t* q_idx, const float* w, int32_t heads, con
       or_index_score(q_idx, w, heads, idx_pages, bt, max_pages, r, pos[i], pos[i] + 1, I + i, M + i);
   }
 }
+
+/* ------------------------------------- bf16 reference of the index score [P1]
+ * "DeepSeek's Attention and KV Cache", "DeepSeek-V4 ... the indexer in four bits": with
+ * the query and key in FP4 the V4 report keeps 99.7 % recall of the top-k.  This is the
+ * same score from the unquantised bf16 query and key, fp64 throughout, for measuring
+ * the recall of the FP4 selection (a reported figure, not a pin). */
+void or_index_score_bf16(const uint16_t* q_idx, const float* w, int32_t heads, const uint16_t* keys, int64_t n,
+                         double* I) {
+  const double scale = 1.0 / sqrt(128.0);
+  for (int64_t s = 0; s < n; ++s) {
+    double acc = 0.0;
+    for (int j = 0; j < heads; ++j) {
+      double dot = 0.0;
+      for (int c = 0; c < OR_DI; ++c)
+        dot += (double)bf16_to_float(q_idx[(int64_t)j * OR_DI + c]) * (double)bf16_to_float(keys[s * OR_DI + c]);
+      double relu = dot * scale > 0.0 ? dot * scale : 0.0;
+      acc += (double)w[j] * relu;
+    }
+    I[s] = acc;
+  }
+}

@@ -165,3 +165,26 @@ def test_attention_special_cases(orc):
     # duplicate (window overlaps selection): counted twice, no de-duplication
     O3, _ = orc.attention(q, np.array([5, 5], np.int32), kv, 0, win, 0, None, None, mp)
     assert np.allclose(O3, np.tile(orc.read_main(kv, 0, 5, None, mp), (3, 1)))
+
+
+def test_fp4_selection_recall_against_bf16_scores(orc):
+    """Recall of the top-512 chosen on FP4 query and key against the top-512 of the bf16
+    score ("DeepSeek-V4": 99.7 % for V4's trained indexer).  On synthetic N(0,1) data the
+    figure is model-free and only reported; it must be far above chance (512 / T)."""
+    import synth
+    T = 6144
+    keys = synth.normal_bf16(880, (T, 128))
+    kv, ix = orc.alloc_pages((T + 127) // 128)
+    orc.pack_kv(synth.normal_bf16(881, (T, 512)), keys, np.zeros(T, np.int32), np.arange(T, dtype=np.int64), kv, ix,
+                None, (T + 127) // 128)
+    rec = []
+    for t in range(3):
+        q = synth.normal_bf16(882 + t, (64, 128))
+        w = np.abs(synth.normal_f32(890 + t, (64,)))   # non-negative head weights, as in a trained indexer's
+        I4, _ = orc.index_score(q, w, ix, 0, 0, T, None, (T + 127) // 128)
+        Ib = orc.index_score_bf16(q, w, keys)
+        a = set(orc.topk(I4.astype(np.float32), 512).tolist())
+        b = set(orc.topk(Ib.astype(np.float32), 512).tolist())
+        rec.append(len(a & b) / 512)
+    print(f"FP4 top-512 recall of the bf16 top-512 (synthetic N(0,1)): {np.round(rec, 3).tolist()}")
+    assert min(rec) > 5 * 512 / T
