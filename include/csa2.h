@@ -204,7 +204,10 @@ const char* csa2_last_error(void);
 
 /* Workspace bytes needed by every call below for n_q queries of up to t_max visible
  * entries with heads_I indexer heads; scores_in_ws != 0 when the caller does not
- * provide a score array (the scores then live in the workspace).  Host-only. */
+ * provide a score array (the scores then live in the workspace).  For small batches
+ * (n_q <= 76) it includes the attention's partial outputs: each query's key tiles are then
+ * split over several CTAs whose fp32 partials a combine kernel merges (under 10 MB).
+ * Host-only. */
 size_t csa2_workspace_bytes(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws);
 
 /* Workspace bytes for the same calls with a candidate pool (csa2_step.pool set): adds
