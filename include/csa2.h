@@ -206,7 +206,7 @@ const char* csa2_last_error(void);
  * entries with heads_I indexer heads; scores_in_ws != 0 when the caller does not
  * provide a score array (the scores then live in the workspace).  For small batches
  * (n_q <= 76) it includes the attention's partial outputs: each query's key tiles are then
- * split over several CTAs whose fp32 partials a combine kernel merges (under 10 MB).
+ * split over several CTAs whose fp32 partials a combine kernel merges (at most about 20 MB).
  * Host-only. */
 size_t csa2_workspace_bytes(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws);
 
