@@ -25,7 +25,7 @@ IDX_E4M3_16, IDX_MXFP4 = 0, 1  # indexer-K formats (csa2_cache.idx_format)
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_DEVICE = range(7)
 TRACE_KINDS = {"pack": 0, "index": 1, "topk_hist": 2, "topk_select": 3, "topk_final": 4, "attn": 5, "topk": 6,
                "pool": 7, "pool_gather": 8, "pool_map": 9, "pool_bmax": 10,
-               "attn_combine": 11}
+               "attn_combine": 11, "pack_window": 12}
 POOL_BLOCK, POOL_BLOCKS, POOL = 8, 2048, 16384  # hierarchical indexer: block, blocks kept, pool positions
 
 

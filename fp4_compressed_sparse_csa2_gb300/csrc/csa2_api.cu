@@ -55,7 +55,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // ------------------------------------------------------------------ tracing
 enum Kind {
   kPack = 0, kIndex = 1, kTopkHist = 2, kTopkSel = 3, kTopkFinal = 4, kAttn = 5, kTopk = 6, kPool = 7, kGather = 8,
-  kMap = 9, kPoolBmax = 10, kAttnCombine = 11, kKinds = 12
+  kMap = 9, kPoolBmax = 10, kAttnCombine = 11, kPackWindow = 12, kKinds = 13
 };
 constexpr int kTraceCap = 4096;
 
@@ -493,7 +493,10 @@ csa2_status csa2_pack_window(const void* rows, const int32_t* req, const int64_t
   a.ring = ring;
   a.n_ring = n_ring;
   a.err = err_word(ws);
-  const cudaError_t e = launch_pack_window(a, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  trace_begin(kPackWindow, s);
+  const cudaError_t e = launch_pack_window(a, s);
+  trace_end(kPackWindow, s);
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "window pack kernel");
 }
 

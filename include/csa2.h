@@ -316,7 +316,7 @@ int64_t csa2_launch_count(void);
  * of kernel `kind` (0 pack/quantise, 1 index score, 2/3/4 histogram, select and final
  * passes of the workspace top-k, 5 attention, 6 cluster top-k, 7 candidate-pool
  * selection, 8 pool gather, 9 pool slot map, 10 pool block maxima, 11 attention split
- * combine); csa2_trace_enable(0) stops and clears. */
+ * combine, 12 FP8 window pack); csa2_trace_enable(0) stops and clears. */
 csa2_status csa2_trace_enable(int32_t on);
 csa2_status csa2_trace_read(int32_t kind, double* total_ms, int64_t* count);
 
