@@ -418,7 +418,7 @@ namespace csa2 {
 
 constexpr int kClCandCap = 4096;   // leader: candidates of the threshold bin
 constexpr int kClLocalCap = 4096;  // per CTA: staged candidates (long rows on 2-CTA clusters stage ~1.5 K)
-constexpr int kClBlockCap = 4096;  // per CTA: block maxima (32-entry blocks) of the chunk
+constexpr int kClBlockCap = 4352;  // per CTA: block maxima (32-entry blocks) of the chunk (133,120-entry chunks fit)
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -1030,6 +1030,18 @@ cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t st
     if (n_act > 0 && n_act >= a.n_q) {
       c = cc;
       break;
+    }
+  }
+  if (c == 1) {
+    // no size holds every row in one wave (many rows, e.g. a prefill chunk): take the
+    // smallest cluster whose chunks fit the block-maximum path, which reads each long row
+    // about once instead of histogramming every key and re-reading the row
+    for (int64_t cc = 1; cc <= 8 && cc <= by_len; cc *= 2) {
+      const int64_t ch = (((a.t_max + cc - 1) / cc + 2047) / 2048) * 2048;
+      if (ch / 32 <= kClBlockCap) {
+        c = cc;
+        break;
+      }
     }
   }
   (void)sm_count;
