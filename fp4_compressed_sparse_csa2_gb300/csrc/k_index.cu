@@ -6,22 +6,24 @@
 // multiplies entirely in FP4.  "From MLA to DSA to HCA/CSA", "CSA: two changes to
 // HCA": the scorer takes ReLU(q . k) * 128^-0.5, weights it per head and sums heads.
 //
-// Design: one persistent CTA per SM (21 warps) over a contiguous range of 128-key
-// tiles (one indexer page each):
+// Design: one persistent CTA per SM (17 warps for N <= 64, 21 for N = 128) over a
+// contiguous range of 128-key tiles (one indexer page each):
 //   warp 0      producer: a 16-page mbarrier ring of bulk copies (147 KB in flight per
 //               SM; the page is stored in the MMA's operand layout), one copy per stage of
 //               adjacent pages, plus one per packed query group;
-//   warps 1-4   TMEM allocator (warp 1) and four MMA issuers: tcgen05.cp of the E4M3 scale
-//               atoms into double-buffered TMEM slots as soon as a page lands, then, once
-//               the accumulator is free, two tcgen05.mma kind::mxf4nvf4 (K = 64 each; MX
-//               scale_vec::2X with E8M0 scales per 32 for MXFP4 pages, 4X with E4M3 per 16
-//               otherwise) into
-//               one of 4 (N <= 64) or 2 (N = 128) fp32 TMEM accumulators D[128 keys][N];
-//   warps 5..20 four epilogue warpgroups taking every fourth tile: tcgen05.ld of one TMEM
-//               row per thread (thread = key), 32 columns at a time; the accumulator goes
-//               back to its issuer as soon as the last columns are in registers.  ReLU,
-//               head weights and head sum use packed fp32x2 FMAs over four partial sums,
-//               then x 128^-0.5 and coalesced fp32 stores.
+//   warps 1-4   TMEM allocator (warp 1) and two MMA issuers (warps 1 and 2): tcgen05.cp of
+//               the scale atoms into double-buffered TMEM slots as soon as a page lands,
+//               then, once the accumulator is free, two tcgen05.mma kind::mxf4nvf4 (K = 64
+//               each; MX scale_vec::2X with E8M0 scales per 32 for MXFP4 pages, 4X with
+//               E4M3 per 16 otherwise) into one of 6 (N <= 64) or 2 (N = 128) fp32 TMEM
+//               accumulators D[128 keys][N];
+//   epilogue    three warpgroups (N <= 64), each alternating between two accumulators so
+//               that it reads one while the other's MMAs run, or four warpgroups in pairs
+//               (N = 128): tcgen05.ld of one TMEM row per thread (thread = key), 32
+//               columns at a time; the accumulator goes back to its issuer as soon as the
+//               last columns are in registers.  ReLU, head weights and head sum use packed
+//               fp32x2 FMAs over four partial sums, then x 128^-0.5 and coalesced fp32
+//               stores.
 // Every wait is bounded; a timeout sets the workspace error word, and the CTA drains
 // its copies and MMAs, frees TMEM and returns.
 #include "csa2_kernels.cuh"
@@ -29,9 +31,15 @@
 
 namespace csa2 {
 
-constexpr uint32_t kIssuers = 4;    // MMA-issuing warps
-constexpr uint32_t kEpiGroups = 4;  // epilogue warpgroups
-constexpr int kIdxThreads = 32 * (1 + kIssuers + 4 * kEpiGroups);  // producer, issuers, epilogue
+constexpr uint32_t kIssuers = 4;    // most MMA-issuing warps (barrier space)
+constexpr uint32_t kEpiGroups = 4;  // epilogue warpgroups (3 in the N <= 64 variant)
+// producer, issuers, epilogue warpgroups
+// MMA issuers (one warp each) and epilogue warpgroups of the N <= 64 and N = 128 variants
+__host__ __device__ constexpr uint32_t idx_issuers(bool split) { return split ? 2u : 3u; }
+__host__ __device__ constexpr uint32_t idx_epi_groups(bool split) { return split ? 4u : 3u; }
+__host__ __device__ constexpr int idx_threads(bool split) {
+  return 32 * (1 + static_cast<int>(idx_issuers(split)) + 4 * static_cast<int>(idx_epi_groups(split)));
+}
 constexpr int kLgStages = 4;
 constexpr int kIdxStages = 1 << kLgStages;  // ring capacity in pages (147 KB); a stage holds n_iss pages
 constexpr float kInvSqrtDI = 0.08838834764831845f;  // 128^-0.5
@@ -75,7 +83,7 @@ __device__ __forceinline__ int64_t seg_page(const Segment& sg, int32_t t) {
 // kMx: MXFP4 pages (8704 B, one E8M0 scale per 32 channels, MX block-scaled MMA);
 // otherwise 9216-byte pages with one E4M3 scale per 16 channels.
 template <bool kSplit, bool kMx>
-__global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a) {
+__global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const IndexArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int S = kIdxStages;
@@ -86,9 +94,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
   uint64_t* bars = reinterpret_cast<uint64_t*>(sw_all + 4 * kEpiGroups * 128);
   uint64_t* full = bars;               // [S]
   uint64_t* empty = full + S;          // [S]
-  uint64_t* acc_full = empty + S;      // [4]
-  uint64_t* acc_empty = acc_full + 4;  // [4]
-  uint64_t* q_full = acc_empty + 4;    // [2]
+  uint64_t* acc_full = empty + S;      // [8]
+  uint64_t* acc_empty = acc_full + 8;  // [8]
+  uint64_t* q_full = acc_empty + 8;    // [2]
   uint64_t* q_empty = q_full + 2;      // [2]
   uint64_t* drain = q_empty + 2;       // [kIssuers]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kIssuers);
@@ -97,22 +105,31 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t N = static_cast<uint32_t>(a.N);
-  const int n_acc = N <= 64 ? 4 : 2;  // TMEM accumulators
-  // Accumulator b serves tiles n with n % n_acc == b.  Each accumulator must always be
-  // handled by the same issuer and the same epilogue warpgroup, so that no waiter can
-  // run two barrier phases ahead (parity waits would alias): the active issuer and
-  // warpgroup counts divide n_acc.
-  const uint32_t n_iss = kIssuers < static_cast<uint32_t>(n_acc) ? kIssuers : static_cast<uint32_t>(n_acc);
-  // N <= 64: warpgroup w serves accumulator w.  N = 128 (two queries of 64 heads): the
-  // four warpgroups pair up, warpgroup w reads the 64 columns (one query) w >> 1 of
-  // accumulator w & 1, so both accumulators keep two warpgroups busy.
+  // TMEM accumulators.  Accumulator b serves tiles n with n % kAcc == b.  Each
+  // accumulator must always be handled by the same issuer and the same epilogue
+  // warpgroup, so that no waiter can run two barrier phases ahead (parity waits would
+  // alias): the active issuer and warpgroup counts divide kAcc.
+  //   N <= 64: six accumulators of N <= 64 columns (0..383); three issuers, issuer i and
+  //     warpgroup i serving accumulators i and i + 3, so the warpgroup reads one
+  //     accumulator while the MMAs of the other one are in flight.  Key scales at
+  //     384..455: each issuer's tiles rotate over three 8-column slots (when tile j's
+  //     scales are copied, only its tiles j - 1 and j - 2 can still be in the tensor
+  //     pipe: the issuer has seen tile j - 3's accumulator released).  Query scales at
+  //     456..503.
+  //   N = 128 (two queries of 64 heads): two accumulators (0..255), key scales at
+  //     256..319, query scales at 320..383; the four warpgroups pair up, warpgroup w
+  //     reads the 64 columns (one query) w >> 1 of accumulator w & 1.
+  constexpr uint32_t kAcc = kSplit ? 2u : 6u;
+  constexpr uint32_t kSfA = kSplit ? 256u : 384u, kSfB = kSplit ? 320u : 456u;
+  constexpr uint32_t n_iss = idx_issuers(kSplit);
+  constexpr uint32_t n_st = kIdxStages / n_iss;  // ring stages of n_iss pages
   constexpr bool split_cols = kSplit;
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);       // the producer's one arrive per stage (plus the copies' bytes)
       mbar_init(&empty[i], n_iss);  // one commit per issuer (one page each)
     }
-    for (int i = 0; i < 4; ++i) {
+    for (uint32_t i = 0; i < kAcc; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], split_cols ? 256 : 128);  // every reader of the accumulator
     }
@@ -151,7 +168,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     // looks up and copies one page, so the lookups overlap.  The per-stage work of this
     // warp is kept to a few dozen instructions: it bounds the rate at which the ring refills.
     const uint64_t pol = policy_evict_first();
-    const uint32_t n_st = kIdxStages / n_iss;
     uint32_t k = 0, ph = 0, n = 0, n_stages = 0, m = 0;
     bool ok = true;
     Segment sg;
@@ -170,7 +186,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
       if (!ok) break;
       ++m;
       for (int32_t t = sg.t0; t < sg.t1;) {
-        const uint32_t in_st = n & (n_iss - 1u);
+        const uint32_t in_st = n % n_iss;
         const int32_t left = sg.t1 - t;
         const int32_t cnt = left < static_cast<int32_t>(n_iss - in_st) ? left : static_cast<int32_t>(n_iss - in_st);
         if (in_st == 0) {
@@ -202,7 +218,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         __syncwarp();
         t += cnt;
         n += static_cast<uint32_t>(cnt);
-        if ((n & (n_iss - 1u)) == 0) {
+        if (n % n_iss == 0) {
           if (lane == 0) mbar_arrive(&full[k]);
           ++n_stages;
           if (++k == n_st) {
@@ -213,7 +229,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
       }
     }
     if (lane == 0) {
-      if (ok && (n & (n_iss - 1u))) {  // partial last stage
+      if (ok && n % n_iss != 0) {  // partial last stage
         mbar_arrive(&full[k]);
         ++n_stages;
       }
@@ -226,18 +242,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         mbar_wait(&full[j % n_st], (j / n_st) & 1u, nullptr);
       for (uint32_t j = (m > 2 ? m - 2 : 0); j < m; ++j) mbar_wait(&q_full[j & 1u], (j >> 1) & 1u, nullptr);
     }
-  } else if (warp >= 1 && warp <= static_cast<int>(kIssuers)) {
+  } else if (warp >= 1 && warp <= static_cast<int>(n_iss)) {
     if (lane == 0 && static_cast<uint32_t>(warp - 1) < n_iss) {
       // ------------------------------------------------------------ MMA issuers
       // issuer i takes the tiles n with n % n_iss == i: a single thread pays ~130 cycles per
-      // dependent tcgen05 op, so four issuers on different warps keep the tensor pipe and
+      // dependent tcgen05 op, so two issuers on different warps keep the tensor pipe and
       // the copy ring moving
       const uint32_t me = static_cast<uint32_t>(warp - 1);
       const uint32_t idesc = idesc_nvf4(128, a.N);
       const uint32_t idesc_mx[2] = {idesc_mxf4(128, a.N, 0u), idesc_mxf4(128, a.N, 2u)};
-      const uint32_t lg_iss = n_iss == 4u ? 2u : (n_iss == 2u ? 1u : 0u);
-      const uint32_t lg_st = kLgStages - lg_iss, lg_acc = n_acc == 4 ? 2u : 1u;
-      uint32_t n = 0, m = 0, cur = 0;
+      uint32_t n = 0, m = 0, cur = 0, j = 0;
       bool ok = true;
       Segment sg;
       for (int64_t g = g_first; ok && g <= g_last; ++g) {
@@ -248,22 +262,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         if (!ok) break;
         tc_fence_after();
         const uint32_t qs = smem_u32(qslot + cur * kIdxPageBytes);
-        const uint32_t sfb = tmem + 320u + 16u * me + 8u * cur;  // 320..383
+        const uint32_t sfb = tmem + kSfB + 16u * me + 8u * cur;
         tmem_cp_sf(sfb, sdesc(qs + nib_q, 128, 128));
         if (!kMx) tmem_cp_sf(sfb + 4, sdesc(qs + nib_q + 512, 128, 128));
         ++m;
         // CTA-local tiles n .. n + len - 1 belong to this segment; this issuer's are the
         // ones with nn % n_iss == me
         const uint32_t len = static_cast<uint32_t>(sg.t1 - sg.t0);
-        for (uint32_t nn = n + ((me - n) & (n_iss - 1u)); nn < n + len; nn += n_iss) {
-          const uint32_t kst = nn >> lg_iss;
-          const uint32_t s = kst & ((1u << lg_st) - 1u), ph = (kst >> lg_st) & 1u;
-          const uint32_t b = nn & static_cast<uint32_t>(n_acc - 1), bph = (nn >> lg_acc) & 1u;
+        for (uint32_t nn = n + (me + n_iss - n % n_iss) % n_iss; nn < n + len; nn += n_iss, ++j) {
+          const uint32_t kst = nn / n_iss;
+          const uint32_t s = kst % n_st, ph = (kst / n_st) & 1u;
+          const uint32_t b = nn % kAcc, bph = (nn / kAcc) & 1u;
           ok = mbar_wait(&full[s], ph, abort);
           if (!ok) break;
           tc_fence_after();
           const uint32_t st = smem_u32(ring + (s * n_iss + me) * kPg);
-          const uint32_t sfa = tmem + 256u + 16u * b + 8u * bph;  // 256..319
+          const uint32_t sfa = tmem + (kSplit ? kSfA + 16u * b + 8u * bph : kSfA + 24u * me + 8u * (j % 3u));
           tmem_cp_sf(sfa, sdesc(st + kIdxNibBytes, 128, 128));
           if (!kMx) tmem_cp_sf(sfa + 4, sdesc(st + kIdxNibBytes + 512, 128, 128));
           ok = mbar_wait(&acc_empty[b], bph ^ 1u, abort);
@@ -292,11 +306,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // thread = TMEM lane = key.  N <= 64: warpgroup wg takes the tiles with n % 4 == wg
+    // thread = TMEM lane = key.  N <= 64: warpgroup wg takes the tiles with n % 3 == wg
     // and every column; N = 128: the tiles with n % 2 == wg % 2 and the 64 columns (the
     // query) wg / 2.
-    const uint32_t wg = static_cast<uint32_t>(warp - 1 - kIssuers) >> 2;
-    const uint32_t wg_step = split_cols ? 2u : 4u, wg_res = split_cols ? (wg & 1u) : wg;
+    const uint32_t wg = static_cast<uint32_t>(warp - 1 - static_cast<int>(n_iss)) >> 2;
+    constexpr uint32_t wg_step = split_cols ? 2u : 3u;
+    const uint32_t wg_res = split_cols ? (wg & 1u) : wg;
     const uint32_t c_lo = split_cols ? 64u * (wg >> 1) : 0u, c_hi = split_cols ? c_lo + 64u : N;
     const int quarter = warp & 3;
     // one leader warp per warpgroup polls the accumulator barrier; the other three park
@@ -304,7 +319,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
     const bool leader = static_cast<uint32_t>(quarter) == ((wg + 1u) & 3u);
     const uint32_t row = static_cast<uint32_t>(quarter * 32 + lane);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float* sw = sw_all + (warp - 1 - kIssuers) * 128;  // this warp's copy of the group's head weights
+    float* sw = sw_all + (warp - 1 - static_cast<int>(n_iss)) * 128;  // this warp's copy of the group's head weights
+    float wr[kSplit ? 1 : 64];  // N <= 64: the group's head weights, one per accumulator column
     uint32_t n = 0, own = 0;
     bool ok = true;
     Segment sg;
@@ -318,12 +334,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         if (q < a.n_q && __ldg(a.req + q) != sg.r) report(a.err, CSA2_ERR_DEVICE, kInfoGroup);
       }
       __syncwarp();
+      if constexpr (!kSplit) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) wr[i] = static_cast<uint32_t>(i) < N ? sw[i] : 0.0f;
+      }
       const int nq = static_cast<int>(a.n_q - q0 < a.G ? a.n_q - q0 : a.G);
       const uint32_t len = static_cast<uint32_t>(sg.t1 - sg.t0);
-      for (uint32_t nn = n + ((wg_res - n) & (wg_step - 1u)); nn < n + len; nn += wg_step) {
+      for (uint32_t nn = n + (wg_res + wg_step - n % wg_step) % wg_step; nn < n + len; nn += wg_step) {
         const int32_t t = sg.t0 + static_cast<int32_t>(nn - n);
-        const uint32_t bb = nn & static_cast<uint32_t>(n_acc - 1);
-        const uint32_t bp = (nn >> (n_acc == 4 ? 2 : 1)) & 1u;
+        const uint32_t bb = nn % kAcc;
+        const uint32_t bp = (nn / kAcc) & 1u;
         const int64_t page = seg_page(sg, t);
         const bool page_ok = page >= 0 && page < a.cache.n_pages;
         volatile int32_t* my_go = go + 2 * wg + (own & 1u);
@@ -342,28 +362,56 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
         const uint32_t hmask = static_cast<uint32_t>(a.heads_I) - 1u;
         const uint32_t lg_h = a.heads_I == 64 ? 6u : 5u;
         float2 acc01 = make_float2(0.0f, 0.0f), acc23 = make_float2(0.0f, 0.0f);
-        for (uint32_t c = c_lo; c < c_hi; c += 32u) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + bb * N + c, r);
-          tmem_ld_wait();
-          if (c + 32u >= c_hi) {
-            tc_fence_before();
-            mbar_arrive(&acc_empty[bb]);
-          }
-          const float4* w4 = reinterpret_cast<const float4*>(sw + c);
+        if constexpr (!kSplit) {
+          // head weights from registers (loaded once per group), two 32-column chunks
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 wv = w4[i];
-            fma2(acc01, make_float2(wv.x, wv.y),
-                 make_float2(fmaxf(__uint_as_float(r[4 * i + 0]), 0.0f), fmaxf(__uint_as_float(r[4 * i + 1]), 0.0f)));
-            fma2(acc23, make_float2(wv.z, wv.w),
-                 make_float2(fmaxf(__uint_as_float(r[4 * i + 2]), 0.0f), fmaxf(__uint_as_float(r[4 * i + 3]), 0.0f)));
+          for (uint32_t cc = 0; cc < 2; ++cc) {
+            if (cc == 1 && N <= 32u) break;
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + bb * N + 32u * cc, r);
+            tmem_ld_wait();
+            if (cc == 1 || N <= 32u) {
+              tc_fence_before();
+              mbar_arrive(&acc_empty[bb]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              fma2(acc01, make_float2(wr[32 * cc + 4 * i + 0], wr[32 * cc + 4 * i + 1]),
+                   make_float2(fmaxf(__uint_as_float(r[4 * i + 0]), 0.0f), fmaxf(__uint_as_float(r[4 * i + 1]), 0.0f)));
+              fma2(acc23, make_float2(wr[32 * cc + 4 * i + 2], wr[32 * cc + 4 * i + 3]),
+                   make_float2(fmaxf(__uint_as_float(r[4 * i + 2]), 0.0f), fmaxf(__uint_as_float(r[4 * i + 3]), 0.0f)));
+            }
+            if (((32u * cc + 32u) & hmask) == 0) {
+              const int gq = static_cast<int>((32u * cc) >> lg_h);
+              if (gq < nq && page_ok && key < (gq == 0 ? sg.nv0 : sg.nv1))
+                a.scores[(q0 + gq) * a.ld + key] = ((acc01.x + acc01.y) + (acc23.x + acc23.y)) * kInvSqrtDI;
+              acc01 = acc23 = make_float2(0.0f, 0.0f);
+            }
           }
-          if (((c + 32u) & hmask) == 0) {
-            const int gq = static_cast<int>(c >> lg_h);
-            if (gq < nq && page_ok && key < (gq == 0 ? sg.nv0 : sg.nv1))
-              a.scores[(q0 + gq) * a.ld + key] = ((acc01.x + acc01.y) + (acc23.x + acc23.y)) * kInvSqrtDI;
-            acc01 = acc23 = make_float2(0.0f, 0.0f);
+        } else {  // N = 128: weights from shared memory (the 19-warp CTA has no registers for them)
+          for (uint32_t c = c_lo; c < c_hi; c += 32u) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + bb * N + c, r);
+            tmem_ld_wait();
+            if (c + 32u >= c_hi) {
+              tc_fence_before();
+              mbar_arrive(&acc_empty[bb]);
+            }
+            const float4* w4 = reinterpret_cast<const float4*>(sw + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 wv = w4[i];
+              fma2(acc01, make_float2(wv.x, wv.y),
+                   make_float2(fmaxf(__uint_as_float(r[4 * i + 0]), 0.0f), fmaxf(__uint_as_float(r[4 * i + 1]), 0.0f)));
+              fma2(acc23, make_float2(wv.z, wv.w),
+                   make_float2(fmaxf(__uint_as_float(r[4 * i + 2]), 0.0f), fmaxf(__uint_as_float(r[4 * i + 3]), 0.0f)));
+            }
+            if (((c + 32u) & hmask) == 0) {
+              const int gq = static_cast<int>(c >> lg_h);
+              if (gq < nq && page_ok && key < (gq == 0 ? sg.nv0 : sg.nv1))
+                a.scores[(q0 + gq) * a.ld + key] = ((acc01.x + acc01.y) + (acc23.x + acc23.y)) * kInvSqrtDI;
+              acc01 = acc23 = make_float2(0.0f, 0.0f);
+            }
           }
         }
       }
@@ -383,7 +431,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_kernel(const IndexArgs a
 size_t index_smem_bytes(int stages) {
   (void)stages;
   return 1024 + static_cast<size_t>(kIdxStages + 2) * kIdxPageBytes + 4 * kEpiGroups * 128 * sizeof(float) +
-         (2 * kIdxStages + 12 + kIssuers) * sizeof(uint64_t) + 16 + 4 * (2 + 2 * kEpiGroups);
+         (2 * kIdxStages + 20 + kIssuers) * sizeof(uint64_t) + 16 + 4 * (2 + 2 * kEpiGroups);
 }
 
 cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream) {
@@ -395,7 +443,8 @@ cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream) {
   cudaError_t e =
       smem_limit_once(reinterpret_cast<const void*>(kernel), smem, limit_set[(split ? 1 : 0) + (mx ? 2 : 0)]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kIdxThreads), smem, stream, nullptr, a);
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(static_cast<unsigned>(idx_threads(split))), smem,
+                    stream, nullptr, a);
 }
 
 }  // namespace csa2
