@@ -6,22 +6,23 @@
 // multiplies entirely in FP4.  "From MLA to DSA to HCA/CSA", "CSA: two changes to
 // HCA": the scorer takes ReLU(q . k) * 128^-0.5, weights it per head and sums heads.
 //
-// Design: one persistent CTA per SM (17 warps for N <= 64, 21 for N = 128) over a
+// Design: one persistent CTA per SM (16 warps for N <= 64, 19 for N = 128) over a
 // contiguous range of 128-key tiles (one indexer page each):
 //   warp 0      producer: a 16-page mbarrier ring of bulk copies (147 KB in flight per
 //               SM; the page is stored in the MMA's operand layout), one copy per stage of
 //               adjacent pages, plus one per packed query group;
-//   warps 1-4   TMEM allocator (warp 1) and two MMA issuers (warps 1 and 2): tcgen05.cp of
-//               the scale atoms into double-buffered TMEM slots as soon as a page lands,
-//               then, once the accumulator is free, two tcgen05.mma kind::mxf4nvf4 (K = 64
-//               each; MX scale_vec::2X with E8M0 scales per 32 for MXFP4 pages, 4X with
-//               E4M3 per 16 otherwise) into one of 6 (N <= 64) or 2 (N = 128) fp32 TMEM
-//               accumulators D[128 keys][N];
+//   issuers     one thread on each of the next three (N <= 64) or two (N = 128) warps,
+//               warp 1 also allocating TMEM: tcgen05.cp of the page's scale atoms into
+//               TMEM slots as soon as a page lands, then, once the accumulator is free,
+//               two tcgen05.mma kind::mxf4nvf4 (K = 64 each; MX scale_vec::2X with E8M0
+//               scales per 32 for MXFP4 pages, 4X with E4M3 per 16 otherwise) into one of
+//               6 (N <= 64) or 2 (N = 128) fp32 TMEM accumulators D[128 keys][N];
 //   epilogue    three warpgroups (N <= 64), each alternating between two accumulators so
 //               that it reads one while the other's MMAs run, or four warpgroups in pairs
 //               (N = 128): tcgen05.ld of one TMEM row per thread (thread = key), 32
 //               columns at a time; the accumulator goes back to its issuer as soon as the
-//               last columns are in registers.  ReLU, head weights and head sum use packed
+//               last columns are in registers.  ReLU, head weights (held in registers for
+//               N <= 64, read from shared memory for N = 128) and head sum use packed
 //               fp32x2 FMAs over four partial sums, then x 128^-0.5 and coalesced fp32
 //               stores.
 // Every wait is bounded; a timeout sets the workspace error word, and the CTA drains
