@@ -121,6 +121,13 @@ def test_index_mx_outliers_peaky(orc, csa2):
     _index_run(orc, csa2, [5, 128, 700], 64, 1, seed=520, qscale=8.0, outliers=0.02)
 
 
+def test_index_mx_many_tiles_per_cta(orc, csa2):
+    """40 requests of 2,000-12,000 MXFP4 entries: about 14 tiles per persistent CTA across
+    group boundaries, so the accumulator rotation and the per-issuer scale slots turn over."""
+    rng = np.random.default_rng(530)
+    _index_run(orc, csa2, [int(x) for x in rng.integers(2000, 12001, size=40)], 64, 1, seed=531)
+
+
 def test_full_mode_over_mx_cache(orc, csa2):
     B, T = 3, 1100
     max_pages = (T + 127) // 128
