@@ -341,10 +341,19 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
       }
       const int nq = static_cast<int>(a.n_q - q0 < a.G ? a.n_q - q0 : a.G);
       const uint32_t len = static_cast<uint32_t>(sg.t1 - sg.t0);
-      for (uint32_t nn = n + (wg_res + wg_step - n % wg_step) % wg_step; nn < n + len; nn += wg_step) {
-        const int32_t t = sg.t0 + static_cast<int32_t>(nn - n);
-        const uint32_t bb = nn % kAcc;
-        const uint32_t bp = (nn / kAcc) & 1u;
+      // this warpgroup's first tile of the segment; its accumulator, phase and tile index
+      // then advance by wg_step tiles per iteration
+      const uint32_t nn0 = n + (wg_res + wg_step - n % wg_step) % wg_step;
+      uint32_t ab = nn0 % kAcc, ap = (nn0 / kAcc) & 1u;
+      int32_t t = sg.t0 + static_cast<int32_t>(nn0 - n);
+      float* const srow = a.scores + q0 * a.ld;  // the group's first score row
+      for (uint32_t nn = nn0; nn < n + len; nn += wg_step, t += static_cast<int32_t>(wg_step)) {
+        const uint32_t bb = ab, bp = ap;
+        ab += wg_step;
+        if (ab >= kAcc) {
+          ab -= kAcc;
+          ap ^= 1u;
+        }
         const int64_t page = seg_page(sg, t);
         const bool page_ok = page >= 0 && page < a.cache.n_pages;
         volatile int32_t* my_go = go + 2 * wg + (own & 1u);
@@ -385,7 +394,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
             if (((32u * cc + 32u) & hmask) == 0) {
               const int gq = static_cast<int>((32u * cc) >> lg_h);
               if (gq < nq && page_ok && key < (gq == 0 ? sg.nv0 : sg.nv1))
-                a.scores[(q0 + gq) * a.ld + key] = ((acc01.x + acc01.y) + (acc23.x + acc23.y)) * kInvSqrtDI;
+                (gq == 0 ? srow : srow + a.ld)[key] = ((acc01.x + acc01.y) + (acc23.x + acc23.y)) * kInvSqrtDI;
               acc01 = acc23 = make_float2(0.0f, 0.0f);
             }
           }
@@ -410,7 +419,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
             if (((c + 32u) & hmask) == 0) {
               const int gq = static_cast<int>(c >> lg_h);
               if (gq < nq && page_ok && key < (gq == 0 ? sg.nv0 : sg.nv1))
-                a.scores[(q0 + gq) * a.ld + key] = ((acc01.x + acc01.y) + (acc23.x + acc23.y)) * kInvSqrtDI;
+                (gq == 0 ? srow : srow + a.ld)[key] = ((acc01.x + acc01.y) + (acc23.x + acc23.y)) * kInvSqrtDI;
               acc01 = acc23 = make_float2(0.0f, 0.0f);
             }
           }
