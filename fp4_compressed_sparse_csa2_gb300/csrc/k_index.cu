@@ -76,8 +76,18 @@ __device__ __forceinline__ bool segment(const IndexArgs& a, int64_t g, int64_t b
   return sg.t0 < sg.t1;
 }
 
-__device__ __forceinline__ int64_t seg_page(const Segment& sg, int32_t t) {
-  return sg.bt_row ? static_cast<int64_t>(__ldg(sg.bt_row + t)) : sg.page_base + t;
+// Named barrier over `count` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // kSplit: N = 128 (two queries of 64 heads per group), handled by warpgroup pairs.
@@ -102,7 +112,6 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
   uint64_t* drain = q_empty + 2;       // [kIssuers]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kIssuers);
   volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
-  volatile int32_t* go = abort + 1;  // [kEpiGroups][2] leader -> warpgroup hand-off
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t N = static_cast<uint32_t>(a.N);
@@ -322,7 +331,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     float* sw = sw_all + (warp - 1 - static_cast<int>(n_iss)) * 128;  // this warp's copy of the group's head weights
     float wr[kSplit ? 1 : 64];  // N <= 64: the group's head weights, one per accumulator column
-    uint32_t n = 0, own = 0;
+    uint32_t n = 0;
     bool ok = true;
     Segment sg;
     for (int64_t g = g_first; ok && g <= g_last; ++g) {
@@ -347,6 +356,9 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
       uint32_t ab = nn0 % kAcc, ap = (nn0 / kAcc) & 1u;
       int32_t t = sg.t0 + static_cast<int32_t>(nn0 - n);
       float* const srow = a.scores + q0 * a.ld;  // the group's first score row
+      // without a block table the segment's pages are adjacent: checked once here
+      const bool seg_pages_ok =
+          sg.bt_row != nullptr || (sg.page_base + sg.t0 >= 0 && sg.page_base + sg.t1 <= a.cache.n_pages);
       for (uint32_t nn = nn0; nn < n + len; nn += wg_step, t += static_cast<int32_t>(wg_step)) {
         const uint32_t bb = ab, bp = ap;
         ab += wg_step;
@@ -354,16 +366,15 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
           ab -= kAcc;
           ap ^= 1u;
         }
-        const int64_t page = seg_page(sg, t);
-        const bool page_ok = page >= 0 && page < a.cache.n_pages;
-        volatile int32_t* my_go = go + 2 * wg + (own & 1u);
-        ++own;
-        if (leader) {
-          const bool got = mbar_wait(&acc_full[bb], bp, abort);
-          if (lane == 0) *my_go = got ? 1 : 0;
+        bool page_ok = seg_pages_ok;
+        if (sg.bt_row != nullptr) {
+          const int64_t page = __ldg(sg.bt_row + t);
+          page_ok = page >= 0 && page < a.cache.n_pages;
         }
-        named_bar_sync(1u + wg, 128u);
-        if (*my_go == 0) {
+        // the leader warp waits for the accumulator; the barrier hands its result to the
+        // other three warps (which wait there without issuing)
+        const bool got = leader ? mbar_wait(&acc_full[bb], bp, abort) : true;
+        if (!named_bar_and(1u + wg, 128u, got)) {
           ok = false;
           break;
         }
@@ -441,7 +452,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
 size_t index_smem_bytes(int stages) {
   (void)stages;
   return 1024 + static_cast<size_t>(kIdxStages + 2) * kIdxPageBytes + 4 * kEpiGroups * 128 * sizeof(float) +
-         (2 * kIdxStages + 20 + kIssuers) * sizeof(uint64_t) + 16 + 4 * (2 + 2 * kEpiGroups);
+         (2 * kIdxStages + 20 + kIssuers) * sizeof(uint64_t) + 16 + 4 * 2;
 }
 
 cudaError_t launch_index(const IndexArgs& a, int grid, cudaStream_t stream) {
