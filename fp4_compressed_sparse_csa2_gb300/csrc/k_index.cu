@@ -32,10 +32,10 @@
 
 namespace csa2 {
 
-constexpr uint32_t kIssuers = 4;    // most MMA-issuing warps (barrier space)
-constexpr uint32_t kEpiGroups = 4;  // epilogue warpgroups (3 in the N <= 64 variant)
-// producer, issuers, epilogue warpgroups
-// MMA issuers (one warp each) and epilogue warpgroups of the N <= 64 and N = 128 variants
+constexpr uint32_t kIssuers = 4;    // upper bound on MMA issuers (drain-barrier space)
+constexpr uint32_t kEpiGroups = 4;  // upper bound on epilogue warpgroups (head-weight space)
+// MMA issuers (one warp each) and epilogue warpgroups of the N <= 64 and N = 128
+// variants; the CTA is the producer warp, the issuer warps and the epilogue warpgroups
 __host__ __device__ constexpr uint32_t idx_issuers(bool split) { return split ? 2u : 3u; }
 __host__ __device__ constexpr uint32_t idx_epi_groups(bool split) { return split ? 4u : 3u; }
 __host__ __device__ constexpr int idx_threads(bool split) {
