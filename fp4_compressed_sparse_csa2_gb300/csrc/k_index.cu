@@ -256,8 +256,8 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
     if (lane == 0 && static_cast<uint32_t>(warp - 1) < n_iss) {
       // ------------------------------------------------------------ MMA issuers
       // issuer i takes the tiles n with n % n_iss == i: a single thread pays ~130 cycles per
-      // dependent tcgen05 op, so two issuers on different warps keep the tensor pipe and
-      // the copy ring moving
+      // dependent tcgen05 op, so the issuers (three, or two for N = 128) sit on different
+      // warps to keep the tensor pipe and the copy ring moving
       const uint32_t me = static_cast<uint32_t>(warp - 1);
       const uint32_t idesc = idesc_nvf4(128, a.N);
       const uint32_t idesc_mx[2] = {idesc_mxf4(128, a.N, 0u), idesc_mxf4(128, a.N, 2u)};
