@@ -172,6 +172,7 @@ class Workload:
         self.cache = csa2.make_cache(self.kv, self.idx, self.max_pages)
         ws0 = csa2.alloc_workspace(1, 64, 0, False, device)
         base = rank_seed_base(rank)
+        self.base = base
         pos = torch.arange(T - 1, dtype=torch.int64, device=device)
         for r in range(B):
             lat = synth.torch_normal_bf16(base + r, (T - 1, D), device)
@@ -215,33 +216,61 @@ class Workload:
 
 
 # ----------------------------------------------------------------------------- oracle sample
-def oracle_sample(wl: "Workload", n_req: int, threads: int):
-    """Time the CPU oracle on the Full-mode step of n_req requests (pack of the new entry,
-    index scores over all T entries, top-512, attention); returns (seconds, requests)."""
+class StepInputs:
+    """The seeded inputs of one Full-mode decode step (the Workload's own draws), made with
+    torch alone: the reference arm needs no CUDA library of this package."""
+
+    def __init__(self, B: int, T: int, rank: int, device):
+        import synth
+        self.B, self.T, self.dev = B, T, device
+        self.max_pages = (T + 127) // 128
+        self.base = rank_seed_base(rank)
+        sb = self.base + 7_000_000
+        self.q = synth.torch_normal_bf16(sb + 1, (B, HEADS, D), device)
+        self.q_idx = synth.torch_normal_bf16(sb + 2, (B, HEADS_I, DI), device)
+        self.w = synth.torch_normal_f32(sb + 3, (B, HEADS_I), device)
+        self.new_lat = synth.torch_normal_bf16(sb + 4, (B, D), device)
+        self.new_key = synth.torch_normal_bf16(sb + 5, (B, DI), device)
+        self.window = synth.torch_normal_bf16(sb + 6, (B * WIN, D), device)
+
+
+def oracle_caches(wl, reqs, threads: int):
+    """The resident caches of the listed requests packed by the oracle, from the same seeded
+    draws as the GPU's (regenerated on the device and copied to the host one request at a
+    time); built outside any timed region."""
     import oracle as orc
     import synth
-    B, T = wl.B, wl.T
-    base = 1000 * 1
-    reqs = list(range(min(n_req, B)))
-    host = {}
-    for r in reqs:   # the same seeded inputs, regenerated on the device and copied to the host
-        lat = synth.torch_normal_bf16(base + r, (T - 1, D), wl.dev)
-        key = synth.torch_normal_bf16(base + r + 50000, (T - 1, DI), wl.dev)
-        host[r] = (lat.view(torch.int16).cpu().numpy().view(np.uint16), key.view(torch.int16).cpu().numpy().view(np.uint16))
+    T = wl.T
     bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    q, q_idx, w = bits(wl.q), bits(wl.q_idx), wl.w.cpu().numpy()
-    new_lat, new_key, window = bits(wl.new_lat), bits(wl.new_key), bits(wl.window)
     caches = {}
 
-    def build(r):    # the resident cache, built outside the timed region
+    def build(r, lat, key):
         kv, ix = orc.alloc_pages(wl.max_pages)
-        lat, key = host[r]
         orc.pack_kv(lat, key, np.zeros(T - 1, np.int32), np.arange(T - 1, dtype=np.int64), kv, ix, None,
                     wl.max_pages)
         caches[r] = (kv, ix)
 
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(build, reqs))
+        futs = []
+        for r in reqs:
+            lat = bits(synth.torch_normal_bf16(wl.base + r, (T - 1, D), wl.dev))
+            key = bits(synth.torch_normal_bf16(wl.base + r + 50000, (T - 1, DI), wl.dev))
+            futs.append(ex.submit(build, r, lat, key))
+            if len(futs) >= threads:        # bounds the host copies in flight
+                futs.pop(0).result()
+        for f in futs:
+            f.result()
+    return caches
+
+
+def oracle_step(wl, caches, threads: int):
+    """Time the CPU oracle on the Full-mode step of the requests in `caches` (pack of the new
+    entry, fp64 index scores over all T entries, top-512, fp64 attention); returns seconds."""
+    import oracle as orc
+    T = wl.T
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    q, q_idx, w = bits(wl.q), bits(wl.q_idx), wl.w.cpu().numpy()
+    new_lat, new_key, window = bits(wl.new_lat), bits(wl.new_key), bits(wl.window)
 
     def one(r):
         kv, ix = caches[r]
@@ -254,8 +283,8 @@ def oracle_sample(wl: "Workload", n_req: int, threads: int):
 
     t0 = time.perf_counter()
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(one, reqs))
-    return time.perf_counter() - t0, len(reqs)
+        list(ex.map(one, sorted(caches)))
+    return time.perf_counter() - t0
 
 
 def profiled_traffic(summary: str, sources, entries: int):
@@ -656,7 +685,8 @@ def run_ours(args, ws, rank, local):
     if rank == 0 and ws == 1 and not args.no_cpu:
         cores = host_cores()
         n_req = min(wl.B, max(4, cores))
-        secs, nr = oracle_sample(wl, n_req, cores)
+        nr = n_req
+        secs = oracle_step(wl, oracle_caches(wl, list(range(n_req)), cores), cores)
         cpu = {"value": round((nr / wl.B) / secs, 6), "unit": UNIT, "cores": min(cores, nr), "kind": "oracle",
                "sample": f"{nr} of {wl.B} requests of the same Full-mode step (pack + fp64 index scores over "
                          f"{wl.T} entries + top-512 + fp64 attention), {secs:.2f} s wall on {min(cores, nr)} "
@@ -690,32 +720,31 @@ def run_ours(args, ws, rank, local):
 
 
 def run_reference(args, ws, rank, local):
-    """The oracle as it stands, on the host cores, timed per step on a bounded sample."""
+    """The oracle as it stands, on the host cores: whole Full-mode layer-steps (every request
+    of the batch), timed one by one.  Inputs are the GPU arm's seeded draws made with torch
+    alone; no CUDA library of this package is loaded."""
     if rank != 0:
         return
-    dev = torch.device("cuda", local) if torch.cuda.is_available() else None
-    if dev is None:
-        print(json.dumps({"impl": "reference", "unavailable": "the reference arm builds its inputs on the GPU"}))
-        return
-    wl = Workload(args.batch, args.ctx, 0, dev)
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    wl = StepInputs(args.batch, args.ctx, 0, dev)
     cores = host_cores()
-    n_req = min(wl.B, max(2, cores // 2))
-    for _ in range(max(0, min(args.warmup, 1))):
-        oracle_sample(wl, 1, 1)
-    times = []
-    for _ in range(max(1, min(args.steps, 3))):
-        secs, nr = oracle_sample(wl, n_req, cores)
-        times.append(secs * wl.B / nr)      # seconds per full 64-request layer-step
+    caches = oracle_caches(wl, list(range(wl.B)), cores)
+    warm = max(0, min(args.warmup, 1))
+    for _ in range(warm):
+        oracle_step(wl, {0: caches[0]}, 1)
+    steps = max(1, min(args.steps, 3))
+    times = [oracle_step(wl, caches, cores) for _ in range(steps)]
     sec = statistics.median(times)
     value = 1.0 / sec
     line = {
-        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": ws, "steps": len(times),
-        "warmup": max(0, min(args.warmup, 1)), "ms_per_step": round(sec * 1000, 2), "higher_is_better": True,
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": warm, "ms_per_step": round(sec * 1000, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
         "data": "synthetic (seeded N(0,1)), same inputs as the GPU arm",
         "config": {"workload": workload_name(wl.B, wl.T), "global_batch": wl.B, "seq_len": wl.T},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": min(cores, n_req), "kind": "oracle",
-                         "sample": f"{n_req} of {wl.B} requests per step, scaled to one {wl.B}-request layer-step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": min(cores, wl.B), "kind": "oracle",
+                         "sample": f"whole layer-steps: all {wl.B} requests per step, {steps} steps timed one by "
+                                   f"one (median), caches packed by the oracle outside the timed region"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

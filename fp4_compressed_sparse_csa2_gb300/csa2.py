@@ -73,6 +73,8 @@ def _load():
         getattr(L, f).argtypes = [ctypes.POINTER(csa2_step), vp, sz, vp]
     L.csa2_topk_noalloc.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp]
     L.csa2_topk_noalloc.restype = ctypes.c_int
+    L.csa2_topk_noalloc_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    L.csa2_topk_noalloc_check.restype = ctypes.c_int
     L.csa2_check.argtypes = [vp, vp, ctypes.POINTER(i32)]
     L.csa2_launch_count.restype = i64
     L.csa2_trace_enable.argtypes = [i32]
@@ -152,6 +154,13 @@ def topk_noalloc(scores, ld, n_visible, n_q, t_max, k, out_idx, stream=None):
     """csa2_topk without a workspace: scratch is a fixed array inside the library (n_q <= 128)."""
     _check(lib.csa2_topk_noalloc(_ptr(scores), int(ld), _ptr(n_visible), int(n_q), int(t_max), int(k),
                                  _ptr(out_idx), _stream(stream)))
+
+
+def topk_noalloc_check(stream=None) -> tuple[int, int]:
+    """(status, info) of the fixed array's error word after the last csa2_topk_noalloc; clears it."""
+    info = ctypes.c_int32(0)
+    st = lib.csa2_topk_noalloc_check(_stream(stream), ctypes.byref(info))
+    return st, info.value
 
 
 def make_step(*, n_q, t_max, q, req, n_visible, window, win_start, win_len, cache, topk_idx, out, q_idx=None,

@@ -631,3 +631,14 @@ extern "C" csa2_status csa2_topk_noalloc(const float* scores, int64_t ld, const 
   if (e != cudaSuccess) return cuda_fail(e, "csa2_topk_noalloc");
   return run_topk(scores, ld, n_visible, n_q, t_max, k, out_idx, scratch + kHeader, err_word(scratch), s);
 }
+
+// Reads and clears the error word of the fixed array behind csa2_topk_noalloc, after the
+// stream has finished: the same report as csa2_check gives for a caller workspace.  It
+// allocates nothing (a synchronous 8-byte copy and clear of the library's own array).
+extern "C" csa2_status csa2_topk_noalloc_check(csa2_stream_t stream, int32_t* info) {
+  uint8_t* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  cudaError_t e = topk_static_scratch(&scratch, &scratch_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_topk_noalloc_check scratch lookup");
+  return csa2_check(scratch, stream, info);
+}

@@ -207,6 +207,11 @@ const char* csa2_last_error(void);
  * provide a score array (the scores then live in the workspace).  For small batches
  * (n_q <= 76) it includes the attention's partial outputs: each query's key tiles are then
  * split over several CTAs whose fp32 partials a combine kernel merges (at most about 20 MB).
+ * Bytes [0, 8) of the workspace are the error word (csa2_check); after a call that scores
+ * (csa2_index_score, Full, Reindex) bytes [256, 256 + ceil(n_q / group) * (N * 64 + 1024))
+ * hold the quantised indexer query, N = group * heads_I rows per group in the
+ * indexer page's operand layout with the scale atoms after the nibbles (N * 64 + 512 with
+ * MXFP4 keys); row n is head n % heads_I of query group * g + n / heads_I.
  * Host-only. */
 size_t csa2_workspace_bytes(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_in_ws);
 
@@ -281,6 +286,13 @@ csa2_status csa2_topk(const float* scores, int64_t ld, const int32_t* n_visible,
  *     csa2_check does not report them. */
 csa2_status csa2_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_visible, int64_t n_q,
                               int64_t t_max, int32_t k, int32_t* out_idx, csa2_stream_t stream);
+
+/* Error word of the last csa2_topk_noalloc call (no counterpart on the pages): synchronises
+ * `stream`, reads and clears the fixed array's error word and reports it as csa2_check
+ * does for a workspace (CSA2_OK, or CSA2_ERR_DEVICE with *info = 3 when a row's counts
+ * disagree between the passes, which overlapping calls on the shared array can cause).
+ * Allocates nothing. */
+csa2_status csa2_topk_noalloc_check(csa2_stream_t stream, int32_t* info);
 
 /* Full mode [P3 section 2 "Full Mode"; P4 "CSA2"]: pack the step's new entries, score
  * the cache with the step's own indexer query, select its own top-512, then run the

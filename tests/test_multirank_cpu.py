@@ -1,7 +1,7 @@
 """The benchmark's multi-rank host path on CPU: two gloo ranks (one process each, started
 with spawn) run the process-group set-up, the max-over-ranks timing reduction, the
-barrier and the reference arm's rank gating (rank 0 alone prints; here, with no GPU, its
-'unavailable' line).  Decode requests are independent, so the replicas exchange nothing
+barrier and the reference arm's rank gating (rank 0 alone runs the oracle, here on a small
+decode of 2 requests x 2,048 entries, and prints the line).  Decode requests are independent, so the replicas exchange nothing
 else; the seeds of their requests must not overlap."""
 import io
 import json
@@ -33,7 +33,8 @@ def _worker(rank: int, port: int, q):
         res["ws"], res["rank"] = ws, r
         res["max"] = bench.max_over_ranks(10.0 * r + 0.25, ws)  # slowest rank's time wins
         bench.barrier(ws)
-        sys.argv = ["bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0"]
+        sys.argv = ["bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+                    "--batch", "2", "--ctx", "2048"]
         args = bench.parse()
         buf = io.StringIO()
         with redirect_stdout(buf):
@@ -66,7 +67,8 @@ def test_two_gloo_ranks_reduce_and_gate_output():
     assert [d["max"] for d in res] == [10.25, 10.25]
     assert res[1]["out"] == ""                              # only rank 0 prints
     line = json.loads(res[0]["out"].strip())
-    assert line["impl"] == "reference" and "unavailable" in line
+    assert line["impl"] == "reference" and line["value"] > 0 and line["n_gpus"] == 2
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
 
 
 def test_replica_seeds_do_not_overlap():

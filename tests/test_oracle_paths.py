@@ -167,6 +167,34 @@ def test_attention_special_cases(orc):
     assert np.allclose(O3, np.tile(orc.read_main(kv, 0, 5, None, mp), (3, 1)))
 
 
+def test_index_score_bf16_one_head_and_linearity(orc):
+    """The bf16 reference score ("DeepSeek-V3.2", the lightning indexer; "From MLA to DSA to
+    HCA/CSA", "CSA" scorer: ReLU of the scaled query-key product, weighted per head and
+    summed) with one head of weight 1 is ReLU(q . k) / sqrt(128) of the unquantised bf16
+    values, computed here with numpy; the full score is then linear in w (which, with the
+    one-head case, fixes every head's term).  A dropped ReLU, a missing 128^-1/2, a
+    transposed operand or a quantised input fails one of these."""
+    T, H = 300, 6
+    keys = synth.normal_bf16(901, (T, 128))
+    q = synth.normal_bf16(902, (H, 128))
+    kf = synth.bf16_to_f32(keys).astype(np.float64)
+    qf = synth.bf16_to_f32(q).astype(np.float64)
+    terms = np.maximum(kf @ qf.T / np.sqrt(128.0), 0.0)          # [T][H] per-head votes
+    assert (terms == 0).any() and (terms > 0).any()              # ReLU active on both sides
+    for j in range(H):
+        Ij = orc.index_score_bf16(np.ascontiguousarray(q[j:j + 1]), np.ones(1, np.float32), keys)
+        assert np.allclose(Ij, terms[:, j], rtol=1e-13, atol=1e-13)
+    w = synth.normal_f32(903, (H,))
+    I = orc.index_score_bf16(q, w, keys)
+    assert np.allclose(I, terms @ w.astype(np.float64), rtol=1e-12, atol=1e-12)
+    # the unquantised score differs from the FP4 one (the inputs are not quantised here)
+    kv, ix = orc.alloc_pages(3)
+    orc.pack_kv(synth.normal_bf16(904, (T, 512)), keys, np.zeros(T, np.int32), np.arange(T, dtype=np.int64), kv, ix,
+                None, 3)
+    I4, _ = orc.index_score(q, w, ix, 0, 0, T, None, 3)
+    assert not np.allclose(I4, I, rtol=1e-6, atol=1e-6)
+
+
 def test_fp4_selection_recall_against_bf16_scores(orc):
     """Recall of the top-512 chosen on FP4 query and key against the top-512 of the bf16
     score ("DeepSeek-V4": 99.7 % for V4's trained indexer).  On synthetic N(0,1) data the
