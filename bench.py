@@ -408,6 +408,34 @@ def _decode_line(csa2, dev, name, B, T, seed, frac=0.0, steps=10, warmup=3, sink
             "kernels_us": kernels, "device_status": st}
 
 
+def mma_peaks(dev):
+    """Tensor-core rates of this library's instruction shapes, measured with the probe
+    kernel (csa2_probe_mma): every SM issues 8,192 MMAs per issuer back to back; TFLOP/s from
+    CUDA events around the launch, MAC per cycle per SM from the kernel's own clock."""
+    from fp4_compressed_sparse_csa2_gb300 import csa2
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
+    out = {}
+    for kind, name, K, shapes in [(1, "nvf4", 64, [(64, 4), (128, 2), (128, 3), (256, 1)]),
+                                  (0, "f16", 16, [(64, 4), (128, 2), (256, 1)])]:
+        for n, iss in shapes:
+            iters = 8192
+            csa2.probe_mma(kind, n, 64, iss, sms, cyc)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            csa2.probe_mma(kind, n, iters, iss, sms, cyc)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            macs = 128 * n * K * iters * iss
+            out[f"{name}_n{n}_i{iss}"] = {"tflops": round(2 * macs * sms / (ms * 1e-3) / 1e12, 1),
+                                          "mac_per_cycle_sm": round(macs / float(cyc.float().median()), 0)}
+    out["nvf4_peak_tflops"] = max(v["tflops"] for k, v in out.items() if k.startswith("nvf4"))
+    out["f16_peak_tflops"] = max(v["tflops"] for k, v in out.items() if k.startswith("f16_"))
+    return out
+
+
 def measure_extra(dev, hbm_peak, bf16_tflops):
     """The other workloads of the layer, each in its own line: the tiny decode, Reuse and
     Reindex at 128 x 262,144, the headline decode with sinks and fused partial RoPE, with the
@@ -537,15 +565,19 @@ def measure_extra(dev, hbm_peak, bf16_tflops):
         st, _ = csa2.check(ws)
         pairs = n * n0 + n * (n + 1) // 2                 # visible (query, entry) pairs
         flops = pairs * HEADS_I * DI * 2
-        fp4_peak = bf16_tflops * 6.0                      # 13.5 / 2.25 nominal ratio
+        del step, ws, cache
+        torch.cuda.empty_cache()
+        probe = mma_peaks(dev)
+        fp4_peak = probe["nvf4_peak_tflops"]
         idx_tf = flops / (kernels.get("index", float("nan")) * 1e-6) / 1e12
         return {"workload": "chunked prefill: 4096 new tokens on 262144 cached entries, index groups of 2",
                 "metric": "chunk-steps/s", "value": round(1000.0 / ms, 3), "ms_per_step": round(ms, 3),
                 "kernels_us": kernels, "index_tflops": round(idx_tf, 1),
                 "index_fp4_frac": round(idx_tf / fp4_peak, 4),
                 "fp4_peak_tflops": round(fp4_peak, 1),
-                "fp4_peak_source": "measured bf16 burst x 6 (the nominal fp4/bf16 dense ratio)",
-                "index_flops": flops, "device_status": st}
+                "fp4_peak_source": "measured: csa2_probe_mma, back-to-back block-scaled NVFP4 tcgen05.mma "
+                                   "(M=128, best of N and issuer counts) on every SM, CUDA events",
+                "mma_probe": probe, "index_flops": flops, "device_status": st}
 
     attempt(prefill)
     return lines

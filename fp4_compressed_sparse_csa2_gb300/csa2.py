@@ -25,7 +25,7 @@ IDX_E4M3_16, IDX_MXFP4 = 0, 1  # indexer-K formats (csa2_cache.idx_format)
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_DEVICE = range(7)
 TRACE_KINDS = {"pack": 0, "index": 1, "topk_hist": 2, "topk_select": 3, "topk_final": 4, "attn": 5, "topk": 6,
                "pool": 7, "pool_gather": 8, "pool_map": 9, "pool_bmax": 10,
-               "attn_combine": 11, "pack_window": 12}
+               "pack_window": 12}
 POOL_BLOCK, POOL_BLOCKS, POOL = 8, 2048, 16384  # hierarchical indexer: block, blocks kept, pool positions
 
 
@@ -73,6 +73,8 @@ def _load():
         getattr(L, f).argtypes = [ctypes.POINTER(csa2_step), vp, sz, vp]
     L.csa2_topk_noalloc.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp]
     L.csa2_topk_noalloc.restype = ctypes.c_int
+    L.csa2_probe_mma.argtypes = [i32, i32, i32, i32, i32, vp, vp]
+    L.csa2_probe_mma.restype = ctypes.c_int
     L.csa2_topk_noalloc_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     L.csa2_topk_noalloc_check.restype = ctypes.c_int
     L.csa2_check.argtypes = [vp, vp, ctypes.POINTER(i32)]
@@ -194,6 +196,12 @@ def check(ws, stream=None) -> tuple[int, int]:
     info = ctypes.c_int32(0)
     st = lib.csa2_check(_ptr(ws), _stream(stream), ctypes.byref(info))
     return st, info.value
+
+
+def probe_mma(kind: int, n: int, iters: int, issuers: int, n_ctas: int, cycles, stream=None):
+    """Tensor-core throughput probe: cycles (int64 [n_ctas], device) per CTA for `iters` MMAs
+    of M = 128 and the given N per issuer (kind 0 f16, 1 NVFP4)."""
+    _check(lib.csa2_probe_mma(int(kind), int(n), int(iters), int(issuers), int(n_ctas), _ptr(cycles), _stream(stream)))
 
 
 def launch_count() -> int:

@@ -55,7 +55,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // ------------------------------------------------------------------ tracing
 enum Kind {
   kPack = 0, kIndex = 1, kTopkHist = 2, kTopkSel = 3, kTopkFinal = 4, kAttn = 5, kTopk = 6, kPool = 7, kGather = 8,
-  kMap = 9, kPoolBmax = 10, kAttnCombine = 11, kPackWindow = 12, kKinds = 13
+  kMap = 9, kPoolBmax = 10, kPackWindow = 12, kKinds = 13
 };
 constexpr int kTraceCap = 4096;
 
@@ -118,8 +118,8 @@ WsLayout ws_layout(int64_t n_q, int32_t heads_I, int64_t t_max, int32_t scores_i
   if (scores_in_ws) off = align256(off + nq * static_cast<size_t>(L.ld) * 4);
   L.topk = off;
   off = align256(off + topk_ws_bytes(n_q));
-  L.apart = off;  // partial outputs of the attention's key-tile splits (small batches)
-  off = align256(off + attn_split_ws_bytes(n_q));
+  L.apart = off;  // partial outputs of the attention's key splits (small batches)
+  off = align256(off + attn_split_ws_bytes(n_q, sm_count()));
   if (pool) {
     L.nb_cap = (t_max + CSA2_POOL_BLOCK - 1) / CSA2_POOL_BLOCK;
     L.bkey = off;
@@ -347,25 +347,17 @@ csa2_status run_attn(const csa2_step& s, uint8_t* base, const WsLayout& L, int32
   a.rope_sin = s.rope_sin;
   a.win_ring = s.win_ring;
   a.win_ring_reqs = s.win_ring_reqs;
-  // small batches split each query's key tiles over several CTAs (plain path only); the
-  // workspace holds the partials for the split count of a 304-SM part at most
+  // small batches split each query's key tiles over a cluster of CTAs
   const bool ext = s.sinks != nullptr || s.rope_cos != nullptr || s.win_ring != nullptr;
-  const int S = std::min(attn_splits(s.n_q, sm_count()), attn_splits(s.n_q, 304));
-  a.splits = ext ? 1 : S;
+  a.splits = attn_splits_for(s.n_q, sm_count(), ext);
   if (a.splits > 1) {
     a.opart = reinterpret_cast<float*>(base + L.apart);
-    a.lpart = a.opart + static_cast<size_t>(s.n_q) * a.splits * CSA2_HEADS * CSA2_D;
+    a.mpart = a.opart + static_cast<size_t>(s.n_q) * a.splits * CSA2_HEADS * CSA2_D;
   }
   trace_begin(kAttn, stream);
-  cudaError_t e = launch_attn(a, stream);
+  const cudaError_t e = launch_attn(a, stream);
   trace_end(kAttn, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel");
-  if (a.splits > 1) {
-    trace_begin(kAttnCombine, stream);
-    e = launch_attn_combine(a, stream);
-    trace_end(kAttnCombine, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "attention combine kernel");
-  }
   return CSA2_OK;
 }
 
@@ -566,6 +558,21 @@ csa2_status csa2_check(void* ws, csa2_stream_t stream, int32_t* info) {
 }
 
 int64_t csa2_launch_count(void) { return g_launches.load(); }
+
+csa2_status csa2_probe_mma(int32_t kind, int32_t n, int32_t iters, int32_t issuers, int32_t n_ctas, int64_t* cycles,
+                           csa2_stream_t stream) {
+  if (kind != 0 && kind != 1) return fail(CSA2_ERR_INVALID_ARG, "kind must be 0 (f16) or 1 (NVFP4)");
+  if (n != 64 && n != 128 && n != 256) return fail(CSA2_ERR_INVALID_ARG, "n must be 64, 128 or 256");
+  if (issuers < 1 || issuers > 4 || issuers * n > 448)
+    return fail(CSA2_ERR_INVALID_ARG, "issuers must be 1..4 with issuers * n <= 448");
+  if (iters < 1 || iters > (1 << 22)) return fail(CSA2_ERR_INVALID_ARG, "iters must be in [1, 2^22]");
+  if (n_ctas < 1 || cycles == nullptr || !aligned(cycles, 8))
+    return fail(CSA2_ERR_INVALID_ARG, "n_ctas >= 1 and an 8-byte aligned cycles array are required");
+  const cudaError_t e = launch_probe_mma(kind, n, iters, issuers, n_ctas, reinterpret_cast<long long*>(cycles),
+                                         reinterpret_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "probe kernel");
+}
 
 csa2_status csa2_trace_enable(int32_t on) {
   std::lock_guard<std::mutex> lk(g_trace.mu);

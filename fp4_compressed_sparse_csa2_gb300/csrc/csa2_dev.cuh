@@ -202,11 +202,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return d;                             // base offset 0, swizzle none
 }
 
-// Instruction descriptor, kind::f16 with bf16 operands and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
-         (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor, kind::f16 with f16 operands (A and B of the same type) and an
+// fp32 accumulator; a_mn_major / b_mn_major select the MN-major operand layouts.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf4nvf4: E2M1 x E2M1, UE4M3 scale per 16 elements.
@@ -224,8 +224,9 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t sf_id) 
          (static_cast<uint32_t>(M >> 4) << 24) | (sf_id << 29);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D (+)= A x B, kind::f16 (operand types in the instruction descriptor).
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
@@ -307,6 +308,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
       "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
@@ -406,35 +416,42 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&x)[16], uint32_t
   return sc;
 }
 
-// 8 packed E2M1 codes (one 32-bit word: code 2i low nibble / 2i+1 high nibble of
-// byte i) times a bf16x2 scale -> 4 bf16x2 words, exactly (a product has at most 6
-// significant bits and lies in [2^-10, 2688]).  Byte lookups with PRMT: the low and
-// high bytes of the bf16 pattern of each magnitude, the sign from the code's bit 3.
-__device__ __forceinline__ void dequant8_bf16(uint32_t w, __nv_bfloat162 scale2, uint32_t (&out)[4]) {
-  // bf16 of magnitudes 0,.5,1,1.5,2,3,4,6: high bytes 00,3F,3F,3F,40,40,40,40;
-  // low bytes 00,00,80,C0,00,40,80,C0.
-  const uint32_t kHiA = 0x3F3F3F00u, kHiB = 0x40404040u;
-  const uint32_t kLoA = 0xC0800000u, kLoB = 0xC0804000u;
+// 8 packed E2M1 codes (one 32-bit word: code 2i in the low nibble, 2i+1 in the high
+// nibble of byte i) times an f16x2 scale -> 4 f16x2 words, exactly: a product has at
+// most 6 significant bits and lies in [2^-10, 2688], inside f16's normal range.  The f16
+// patterns of the magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 have a zero low byte, so one byte
+// lookup (PRMT) per four codes gives the high bytes; the sign comes from each code's bit 3.
+__device__ __forceinline__ void dequant8_f16(uint32_t w, uint32_t scale2, uint32_t (&out)[4]) {
+  const uint32_t kHiA = 0x3E3C3800u, kHiB = 0x46444240u;  // high bytes of 0,.5,1,1.5 | 2,3,4,6
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const uint32_t c = (w >> (16 * half)) & 0xFFFFu;  // 4 codes e0..e3 in nibbles
-    const uint32_t sel = c & 0x7777u;
-    uint32_t lo, hi, sg;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(kLoA), "r"(kLoB), "r"(sel));
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(kHiA), "r"(kHiB), "r"(sel));
-    // sign bytes: replicate the msb of bytes holding each code's sign bit
+    uint32_t hi, sg, w0, w1;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(kHiA), "r"(kHiB), "r"(c & 0x7777u));
+    // byte k of sg: 0xFF when code k is negative (sign-replicating selectors)
     asm("prmt.b32 %0, %1, %2, 0xD9C8;" : "=r"(sg) : "r"(c << 4), "r"(c));
     hi |= sg & 0x80808080u;
-    uint32_t w0, w1;
-    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(w0) : "r"(lo), "r"(hi));
-    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(w1) : "r"(lo), "r"(hi));
-    __nv_bfloat162 v0 = *reinterpret_cast<__nv_bfloat162*>(&w0);
-    __nv_bfloat162 v1 = *reinterpret_cast<__nv_bfloat162*>(&w1);
-    v0 = __hmul2(v0, scale2);
-    v1 = __hmul2(v1, scale2);
-    out[2 * half] = *reinterpret_cast<uint32_t*>(&v0);
-    out[2 * half + 1] = *reinterpret_cast<uint32_t*>(&v1);
+    // f16 k = high byte k over a zero low byte
+    asm("prmt.b32 %0, %1, %2, 0x1404;" : "=r"(w0) : "r"(hi), "r"(0u));
+    asm("prmt.b32 %0, %1, %2, 0x3424;" : "=r"(w1) : "r"(hi), "r"(0u));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[2 * half]) : "r"(w0), "r"(scale2));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[2 * half + 1]) : "r"(w1), "r"(scale2));
   }
+}
+
+// Two E4M3 codes (low byte first) -> f16x2 bits, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2_bits(uint32_t two) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(two));
+  return r;
+}
+
+// Two fp32 values -> f16x2 bits (lo in the low half), round to nearest, saturated to the
+// finite f16 range.
+__device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // ----------------------------------------------------------------- cache layout

@@ -82,26 +82,26 @@ struct AttnArgs {
   const float* rope_sin;
   const uint8_t* win_ring;  // FP8 window ring [win_ring_reqs][128][528] or nullptr
   int32_t win_ring_reqs;
-  // split over the key tiles (plain path only): splits CTAs per (query, head half), each
-  // over a run of the tile list [window, selected 0..3]; they write normalised fp32
-  // partial outputs and log2 sum-exps that attn_combine_kernel merges
-  int32_t splits;  // 1 = no split (the output is written directly)
-  float* opart;    // [n_q][splits][64][512]
-  float* lpart;    // [n_q][splits][64]
+  // key splits: `splits` CTAs per query (one thread-block cluster) each take a run of the
+  // tile list [window, selected 0..3]; they write raw partial outputs and per-head (max,
+  // sum) to the workspace and combine them after a cluster barrier; 1 = one CTA per query
+  int32_t splits;
+  float* opart;  // [n_q * splits][64][512] (splits > 1)
+  float* mpart;  // [n_q * splits][2][64]
 };
 
-// Key-tile splits per (query, head half) for n_q queries on sm_count SMs: the most (up to
-// the 5 tiles) that keep all CTAs in one wave; 1 when two CTAs per query already fill it.
+// Upper bound on the key splits of one query (its five 128-key tiles).
 constexpr int kAttnMaxSplits = 5;
-inline int attn_splits(int64_t n_q, int sm_count) {
+// Key splits that keep n_q queries' CTAs in one wave on sm_count SMs (before the cluster
+// occupancy check), and the workspace bytes of their partials.
+inline int attn_wave_splits(int64_t n_q, int sm_count) {
   if (n_q <= 0) return 1;
-  const int64_t s = sm_count / (2 * n_q);
+  const int64_t s = sm_count / n_q;
   return static_cast<int>(s < 1 ? 1 : (s > kAttnMaxSplits ? kAttnMaxSplits : s));
 }
-// Workspace bytes for the partial outputs of n_q queries (sized for up to 304 SMs).
-inline size_t attn_split_ws_bytes(int64_t n_q) {
-  const int s = attn_splits(n_q, 304);
-  return s > 1 ? static_cast<size_t>(n_q) * s * 64 * (512 + 1) * sizeof(float) : 0;
+inline size_t attn_split_ws_bytes(int64_t n_q, int sm_count) {
+  const int s = attn_wave_splits(n_q, sm_count);
+  return s > 1 ? static_cast<size_t>(n_q) * s * 64 * (512 + 2) * sizeof(float) : 0;
 }
 
 struct WinPackArgs {
@@ -183,9 +183,13 @@ cudaError_t smem_limit_once(const void* kernel, size_t bytes, std::atomic<int>* 
 cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes);
 cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream);
 size_t attn_smem_bytes();
-cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);          // a.splits > 1: then the combine
-cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream);  // merges the key-tile splits
+// Key splits per query for n_q queries on sm_count SMs: the most (up to 5) that keep all CTAs
+// in one wave and that the device can hold as one cluster (ext: the optional-feature kernel).
+int attn_splits_for(int64_t n_q, int sm_count, bool ext);
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_pack_window(const WinPackArgs& a, cudaStream_t stream);
+cudaError_t launch_probe_mma(int32_t kind, int32_t n, int32_t iters, int32_t issuers, int32_t n_ctas,
+                             long long* cycles, cudaStream_t stream);
 cudaError_t launch_pool_bmax(const PoolArgs& a, cudaStream_t stream);  // block maxima (first)
 cudaError_t launch_pool(const PoolArgs& a, cudaStream_t stream);       // the selection
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);

@@ -6,43 +6,58 @@
 // the FP4 entries are dequantised before attention.  "From MLA to DSA to HCA/CSA",
 // "What replaced MLA": attention(q, kv, kv) with K and V the same tensor.
 //
-// Design: two CTAs of 8 warps per query, each owning 32 of the 64 heads (heads are
-// independent, so the halves exchange nothing); 5 key tiles of 128 keys, the window
-// tile first:
-//   prefetch the 288-byte records of the next selected tile go to a raw staging buffer
-//            with cp.async while the current tile is processed; the window rows (bf16)
-//            are copied straight into the key tile at the start;
-//   build    all warps dequantise the staged records (byte-permute lookups, exact bf16
-//            products) into the bf16 key tile in the tensor-core operand layout;
-//   S^T      two threads issue 32 tcgen05.mma kind::f16 (M = 128 keys, N = 32 heads,
-//            K = 512) into four partial TMEM sums;
-//   softmax  thread = key, 16 heads per thread: warp max reductions, a per-head
-//            reference max that only moves when a tile exceeds it by 2^8 (then the
-//            TMEM accumulator and the running sums are rescaled), exp2, bf16 P^T to
-//            shared memory;
-//   O^T      32 tcgen05.mma (4 M-tiles of 128 output channels, N = 32 heads, K = 128
-//            keys) reading the SAME bf16 tile as an MN-major operand (K == V);
-//   epilogue O = O^T / l per head -> bf16, lse = ln(sum exp).
+// Design: one CTA of 16 warps per (query, key split), all 64 heads, so every selected
+// record is dequantised once.  A query's key tiles are [window, selected 0..3] (128 keys
+// each); S CTAs of a thread-block cluster take consecutive runs of them and merge their
+// partial outputs through L2 after a cluster barrier (S = 1 needs no merge).
+//   operands  f16: the dequantised entries (e2m1 x e4m3 products are exact in f16), the
+//             window rows and the queries (bf16 -> f16 is exact in f16's range), and the
+//             probabilities P (8 more bits than bf16);
+//   tile      one f16 K = V buffer [128 keys][512] in the core-matrix layout, seen as four
+//             128-channel chunks.  The O MMAs of tile t free the chunks one by one, and
+//             tile t+1 is dequantised into each freed chunk (its records were loaded into
+//             registers one tile ahead) while the later O chunks and the S MMAs of the
+//             chunks already built run on the tensor pipe;
+//   S^T      tcgen05.mma kind::f16, M = 128 keys, N = 64 heads, K = 512 (TMEM cols 256..319);
+//   softmax  thread = key, 16 heads per thread: a block-wide vote finds whether any score
+//             exceeds its head's reference maximum by 2^8; only then are the reference
+//             maxima raised (warp max reductions) and O^T and the running sums rescaled;
+//   O^T      += V^T P^T: 4 output chunks of 128 channels x 64 heads (TMEM cols 0..255)
+//             reading the same tile as an MN-major operand (K == V);
+//   epilogue O = O^T / l per head -> bf16 and lse; with S > 1 each CTA writes its raw
+//             partial and its (max, sum) per head to the workspace, one cluster barrier
+//             orders them, and each CTA of the cluster combines one slice of the heads.
 // Optional, from "From MLA to DSA to HCA/CSA": per-head attention sinks (a logit that
 // joins the softmax denominator and has no value; section "The sliding window") and
 // the partial RoPE of "What replaced MLA" (the queries' trailing 64 channels rotated
-// in shared memory before the first S^T MMA; the output's rotated back with the
-// negated angle before it is rounded to bf16).
+// before the first S^T MMA; the output's rotated back with the negated angle before it
+// is rounded to bf16), and windows read from the FP8 ring.
 #include "csa2_kernels.cuh"
 
 namespace csa2 {
 
-constexpr int kAttnThreads = 256;
-constexpr int kHeads = 64;                          // query heads
-constexpr int kHH = 32;                             // heads per CTA
-constexpr uint32_t kKtBytes = 128 * 512 * 2;        // bf16 key tile
-constexpr uint32_t kQsBytes = kHH * 512 * 2;        // bf16 queries of this CTA's heads
-constexpr uint32_t kPsBytes = 128 * kHH * 2;        // bf16 P^T
-constexpr uint32_t kRawBytes = 128 * kKvBytes;      // staged FP4 records of one tile
-constexpr uint32_t kOCols = 0, kSCols = 256;        // TMEM columns: O^T 4 x 32, S^T 4 partial sums x 32
-constexpr float kRescaleThreshold = 8.0f;      // log2 units
+constexpr int kComputeWarps = 16;  // softmax, tile build, epilogue; lane 0 of warps 0..3 issues MMAs
+constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kAttnThreads = kComputeThreads;
+constexpr int kHeads = 64;
+constexpr uint32_t kKtBytes = 128 * 512 * 2;  // f16 key/value tile
+constexpr uint32_t kQsBytes = 64 * 512 * 2;   // f16 queries, all heads
+constexpr uint32_t kPsBytes = 128 * 64 * 2;   // f16 P^T
+constexpr uint32_t kSCol = 256;               // TMEM: O^T chunk c at columns 64c.., S^T partial c at 256 + 64c
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+// shared memory map (bytes)
+constexpr uint32_t kOffQs = kKtBytes;
+constexpr uint32_t kOffPs = kOffQs + kQsBytes;
+constexpr uint32_t kOffRec = kOffPs + kPsBytes;     // int32 [512] record ids (page * 128 + slot), -1 = none
+constexpr uint32_t kOffCnt = kOffRec + 512 * 4;     // int32 [4] valid entries per selected tile
+constexpr uint32_t kOffAlpha = kOffCnt + 16;        // f32 [64] per-head factor
+constexpr uint32_t kOffRef = kOffAlpha + 64 * 4;    // f32 [64] reference maximum (log2 units)
+constexpr uint32_t kOffMl = kOffRef + 64 * 4;       // f32 [2][64] (max, sum) published to the cluster
+constexpr uint32_t kOffBar = kOffMl + 128 * 4;      // u64 s_bar, o_bar[4], drain
+constexpr uint32_t kOffMisc = kOffBar + 6 * 8;      // u32 tmem slot, i32 abort flag, 2 spare
+constexpr uint32_t kAttnSmem = kOffMisc + 16;
 
-// Offset of element (row, col) in a [rows][512] bf16 operand tile stored as 8x8 core
+// Offset of element (row, col) in a [rows][512] 16-bit operand tile stored as 8x8 core
 // matrices: row groups of 8 at 8192-byte stride, 8-column chunks at 128-byte stride.
 __device__ __forceinline__ uint32_t tile_off(uint32_t row, uint32_t col) {
   return (row >> 3) * 8192u + (col >> 3) * 128u + (row & 7u) * 16u + (col & 7u) * 2u;
@@ -61,464 +76,652 @@ __device__ __forceinline__ void tile_item(uint32_t c, uint32_t rows, uint32_t& r
 __device__ __forceinline__ void cp_async16(uint32_t sdst, const void* gsrc, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sdst), "l"(gsrc), "r"(src_bytes) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-
-// E4M3 code -> bf16 (exact: 4 significant bits, range 2^-9 .. 448), both halves.
-__device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
-  const uint32_t e = (code >> 3) & 15u, m = code & 7u;
-  uint32_t bits = e ? (((e + 120u) << 7) | (m << 4)) : (__float_as_uint(static_cast<float>(m) * 0.001953125f) >> 16);
-  bits |= (code & 0x80u) << 8;
-  const uint32_t both = bits | (bits << 16);
-  return *reinterpret_cast<const __nv_bfloat162*>(&both);
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
 }
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_newest_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// Barrier over every thread of the cluster; release/acquire orders the partials each CTA
+// wrote to global memory before it.
+__device__ __forceinline__ void attn_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Per-head sum of the four lane quarters' partial sums ([4][64] in shared memory).
+__device__ __forceinline__ float lred_sum(const float* lred, int h) {
+  return lred[h] + lred[64 + h] + lred[128 + h] + lred[192 + h];
+}
+
+// Named barrier 1 over the CTA's 512 threads, and its OR-reduction form.
+__device__ __forceinline__ void cbar_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+__device__ __forceinline__ bool cbar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.or.pred p, 1, 512, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
 
 // kExt: the optional features (sinks, partial RoPE, FP8 window ring) are compiled in;
-// the plain instance carries none of their code.  kSplit (plain path only): a.splits CTAs
-// per (query, head half) each take a run of the key tiles and write a partial.
-template <bool kExt, bool kSplit>
+// the plain instance carries none of their code.
+template <bool kExt>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* Kt = smem;
-  uint8_t* Qs = Kt + kKtBytes;
-  uint8_t* Ps = Qs + kQsBytes;
-  uint8_t* Raw = Ps + kPsBytes;
-  float* ref = reinterpret_cast<float*>(Raw + kRawBytes);  // [32] reference max (log2 units)
-  float* alpha = ref + kHH;                                 // [32]
-  float* tmax = alpha + kHH;                                // [4][32]
-  float* lred = tmax + 4 * kHH;                             // [4][32]
-  int64_t* recoff = reinterpret_cast<int64_t*>(lred + 4 * kHH);        // [512] record byte offsets, -1 = none
-  int32_t* tile_cnt = reinterpret_cast<int32_t*>(recoff + CSA2_TOPK);  // [4] valid entries per selected tile
-  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(tile_cnt + 4);  // [2] one per MMA issuer
-  uint64_t* drain = mma_bar + 2;                                    // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
-  int32_t* flags = reinterpret_cast<int32_t*>(tmem_slot + 1);  // [0] abort, [1] rescale
+  uint8_t* Qs = smem + kOffQs;
+  uint8_t* Ps = smem + kOffPs;
+  int32_t* recid = reinterpret_cast<int32_t*>(smem + kOffRec);
+  int32_t* tile_cnt = reinterpret_cast<int32_t*>(smem + kOffCnt);
+  float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* ref_s = reinterpret_cast<float*>(smem + kOffRef);
+  float* ml = reinterpret_cast<float*>(smem + kOffMl);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kOffBar);  // S of a tile complete
+  uint64_t* o_bar = s_bar + 1;                                     // [4] O chunk c complete
+  uint64_t* drain = s_bar + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = kSplit ? a.splits : 1;  // CTAs per (query, head half), each over a run of tiles
-  const int64_t qi = blockIdx.x / (2 * S);
-  const int sp = static_cast<int>((blockIdx.x >> 1) % S);
-  const int h0 = (blockIdx.x & 1) * kHH;  // first head of this CTA
+  // MMA issuers: lane 0 of warps 0..3; issuer c owns 128-channel chunk c (its S partial sum
+  // and its O chunk), so no two issuers accumulate into one TMEM region
+  const bool issuer = warp < 4 && lane == 0;
+  const int qd = warp & 3;   // TMEM lane quarter of this warp
+  const int hg = warp >> 2;  // head group: heads [16 hg, 16 hg + 16) in the softmax, O chunk hg
+  const int S = a.splits;    // CTAs per query (one cluster)
+  const int64_t qi = blockIdx.x / S;
+  const int sp = static_cast<int>(blockIdx.x % S);  // rank in the cluster
   // this CTA's run [t_lo, t_hi) of the tile list [window, selected 0, 1, 2, 3]
   const int t_lo = sp * 5 / S, t_hi = (sp + 1) * 5 / S;
   const bool has_win = t_lo == 0;
-  const int sel_lo = t_lo == 0 ? 0 : t_lo - 1, sel_hi = t_hi - 1;  // selected tiles [sel_lo, sel_hi)
+  const int sel_lo = has_win ? 0 : t_lo - 1, sel_hi = t_hi - 1;  // selected tiles [sel_lo, sel_hi)
   const int32_t nv = __ldg(a.n_visible + qi);
-  const int32_t wl = max(0, min(CSA2_WIN, __ldg(a.win_len + qi)));
+  const int32_t wl = has_win ? max(0, min(CSA2_WIN, __ldg(a.win_len + qi))) : 0;
+  const bool ring = kExt && a.win_ring != nullptr;
+  const bool rope = kExt && a.rope_cos != nullptr;
+  const bool win_tile = has_win && wl > 0;  // an empty window is no tile
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&mma_bar[i], 1);
-      mbar_init(&drain[i], 1);
-    }
-    flags[0] = 0;
-    flags[1] = 0;
+    mbar_init(s_bar, 4);  // one commit per issuer
+    for (int i = 0; i < 4; ++i) mbar_init(&o_bar[i], 1);
+    mbar_init(drain, 1);
+    *abort = 0;
     fence_mbar_init();
   }
-  if (tid < kHH) ref[tid] = -INFINITY;
   if (warp == 0) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   pdl_trigger();
-  // queries of this CTA's heads, then the window rows, -> shared memory (operand
-  // layout, K-major over the 512 channels); two cp.async groups
+  // The queries go to registers and the window's bf16 rows (for the window's CTA) to the
+  // key tile with cp.async: both are this call's inputs, so the loads overlap the previous
+  // kernel's tail.  The f16 conversion follows (the window's chunk by chunk, in place).
+  uint4 qv[8];
   {
-    const __nv_bfloat16* qg = a.q + (qi * kHeads + h0) * CSA2_D;
-    for (int c = tid; c < kHH * 64; c += kAttnThreads) {
+    const __nv_bfloat16* qg = a.q + qi * kHeads * CSA2_D;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
       uint32_t h, ch;
-      tile_item(static_cast<uint32_t>(c), kHH, h, ch);
-      cp_async16(smem_u32(Qs + tile_off(h, ch * 8)), qg + h * CSA2_D + ch * 8, 16);
+      tile_item(static_cast<uint32_t>(tid + kComputeThreads * i), kHeads, h, ch);
+      qv[i] = __ldg(reinterpret_cast<const uint4*>(qg + h * CSA2_D + ch * 8));
     }
-    cp_async_commit();
-    const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
-    const bool bf16_rows = (!kExt || a.win_ring == nullptr) && has_win;
-    for (int c = tid; bf16_rows && c < 128 * 64; c += kAttnThreads) {  // bf16 window rows
-      uint32_t r, ch;
-      tile_item(static_cast<uint32_t>(c), 128, r, ch);
-      const bool ok = static_cast<int32_t>(r) < wl;
-      cp_async16(smem_u32(Kt + tile_off(r, ch * 8)), ok ? static_cast<const void*>(wg + r * CSA2_D + ch * 8)
-                                                         : static_cast<const void*>(a.window),
-                 ok ? 16u : 0u);
-    }
-    cp_async_commit();
-  }
-  // The copies above read only this call's inputs, so they overlap the previous kernel's
-  // tail; the selected indices (and in Full mode the new entries) come from earlier kernels.
-  pdl_wait();
-  // offsets of the 512 selected records (one round trip for all indices)
-  if (tid < 4) tile_cnt[tid] = 0;
-  __syncthreads();
-  {
-    const int32_t r = __ldg(a.req + qi);
-    for (int i = tid; i < CSA2_TOPK; i += kAttnThreads) {
-      const int32_t e = __ldg(a.topk_idx + qi * CSA2_TOPK + i);
-      int64_t off = -1;
-      if (e >= 0) {
-        const int64_t pg = e < nv ? page_id(a.cache, r, e) : -1;
-        if (pg >= 0 && pg < a.cache.n_pages)
-          off = pg * kKvPageBytes + static_cast<int64_t>(e % kPage) * kKvBytes;
-        else
-          report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
+    if (win_tile && !ring) {
+      const __nv_bfloat16* wg = a.window + __ldg(a.win_start + qi) * CSA2_D;
+      for (int c = tid; c < 128 * 64; c += kComputeThreads) {
+        uint32_t r, ch;
+        tile_item(static_cast<uint32_t>(c), 128, r, ch);
+        const bool ok = static_cast<int32_t>(r) < wl;
+        cp_async16(smem_u32(Kt + tile_off(r, ch * 8)),
+                   ok ? static_cast<const void*>(wg + r * CSA2_D + ch * 8) : static_cast<const void*>(a.window),
+                   ok ? 16u : 0u);
       }
-      recoff[i] = off;
-      if (off >= 0) atomicAdd(&tile_cnt[i >> 7], 1);
+      cp_async_commit();
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t idesc_s = idesc_bf16(128, kHH, 0, 0);
-  const uint32_t idesc_o = idesc_bf16(128, kHH, 1, 1);
-
-  // Stages the records of selected tile t (16-byte pieces; a missing record reads as zeros).
-  auto prefetch = [&](int t) {
-    for (int c = tid; c < 128 * (kKvBytes / 16); c += kAttnThreads) {
-      const int slot = c / (kKvBytes / 16), j = c - slot * (kKvBytes / 16);
-      const int64_t off = recoff[t * 128 + slot];
-      cp_async16(smem_u32(Raw + slot * kKvBytes + j * 16), a.cache.kv + (off >= 0 ? off + j * 16 : 0),
-                 off >= 0 ? 16u : 0u);
-    }
-    cp_async_commit();
+  // the selected indices (and in Full mode the new entries, or the window ring) come from
+  // earlier kernels
+  pdl_wait();
+  const int tsel = tid >> 7;  // 512 compute threads: one selected slot each
+  const bool mine = tsel >= sel_lo && tsel < sel_hi;
+  const int32_t e_sel = mine ? __ldg(a.topk_idx + qi * CSA2_TOPK + tid) : -1;
+  if (tid < 4) tile_cnt[tid] = 0;
+  auto cvt16 = [](uint4 v) {  // 8 bf16 -> 8 f16
+    return make_uint4(f16x2_sat(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u)),
+                      f16x2_sat(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)),
+                      f16x2_sat(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u)),
+                      f16x2_sat(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u)));
   };
-  auto next_selected = [&](int t) {  // first selected tile of this run after t with any entry, or 4
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t h, ch;
+    tile_item(static_cast<uint32_t>(tid + kComputeThreads * i), kHeads, h, ch);
+    *reinterpret_cast<uint4*>(Qs + tile_off(h, ch * 8)) = cvt16(qv[i]);
+  }
+  __syncthreads();  // tile_cnt cleared
+  {
+    int32_t rid = -1;
+    if (e_sel >= 0) {
+      const int64_t pg = e_sel < nv ? page_id(a.cache, __ldg(a.req + qi), e_sel) : -1;
+      if (pg >= 0 && pg < a.cache.n_pages && pg < (int64_t(1) << 24))
+        rid = static_cast<int32_t>(pg * kPage + e_sel % kPage);
+      else
+        report(a.err, CSA2_ERR_DEVICE, kInfoTopkIdx);
+    }
+    recid[tid] = rid;
+    if (rid >= 0) atomicAdd(&tile_cnt[tsel], 1);
+  }
+  if (kExt && win_tile && ring) {
+    // FP8 window ring: row i of the tile is the entry of position newest - i; E4M3 -> f16 in
+    // hardware (exact), times the block's 2^e in fp32, -> f16
+    const int64_t newest = __ldg(a.win_start + qi);
+    const int32_t r = __ldg(a.req + qi);
+    const bool ring_ok = r >= 0 && r < a.win_ring_reqs && newest - wl + 1 >= 0;
+    if (!ring_ok && tid == 0) report(a.err, CSA2_ERR_DEVICE, kInfoPos);
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t task = static_cast<uint32_t>(tid + kComputeThreads * i);
+      const uint32_t row = (task & 7u) | (((task >> 5) & 15u) << 3);
+      const uint32_t j = ((task >> 3) & 3u) | ((task >> 9) << 2);  // 32-channel block
+      uint8_t* dst = Kt + tile_off(row, 32 * j);
+      if (!ring_ok || static_cast<int32_t>(row) >= wl) {  // no entry: zeros (masked)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + m * 128) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const int64_t pos = newest - row;
+      const uint8_t* rec = a.win_ring + (static_cast<int64_t>(r) * CSA2_WIN + pos % CSA2_WIN) * CSA2_WIN_BYTES;
+      const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(rec + 32 * j));
+      const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(rec + 32 * j + 16));
+      const float sc = ldexpf(1.0f, static_cast<int>(__ldg(rec + 512 + j)) - 127);
+      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(e4m3x2_f16x2((cw[2 * m + (k >> 1)] >> (16 * (k & 1))) & 0xFFFFu));
+          o[k] = f16x2_sat(f.x * sc, f.y * sc);
+        }
+        *reinterpret_cast<uint4*>(dst + m * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+  if (tid < kHeads) ref_s[tid] = -INFINITY;
+  tc_fence_before();
+  __syncthreads();  // record ids, tile counts, converted queries (and the ring window)
+  tc_fence_after();
+  if (rope) {
+    // q = q cos + rotate_half(q) sin on channels 448 + i / 480 + i (angle i), in f16 after
+    // the conversion (one rounding of the fp32 rotation of the exact inputs)
+    for (int p = tid; p < kHeads * 32; p += kAttnThreads) {
+      const uint32_t h = static_cast<uint32_t>(p) >> 5, i = static_cast<uint32_t>(p) & 31u;
+      const float c = __ldg(a.rope_cos + qi * 32 + i), sn = __ldg(a.rope_sin + qi * 32 + i);
+      __half* pa = reinterpret_cast<__half*>(Qs + tile_off(h, 448u + i));
+      __half* pb = reinterpret_cast<__half*>(Qs + tile_off(h, 480u + i));
+      const float x = __half2float(*pa), y = __half2float(*pb);
+      const uint32_t two = f16x2_sat(x * c - y * sn, y * c + x * sn);
+      *reinterpret_cast<uint16_t*>(pa) = static_cast<uint16_t>(two & 0xFFFFu);
+      *reinterpret_cast<uint16_t*>(pb) = static_cast<uint16_t>(two >> 16);
+    }
+    __syncthreads();
+  }
+  const uint32_t tmem = *tmem_slot;
+
+  auto next_sel = [&](int t) {  // first selected tile of this run after t with an entry, or -1
     int u = t + 1;
     while (u < sel_hi && tile_cnt[u] == 0) ++u;
-    return u < sel_hi ? u : 4;
+    return u < sel_hi ? u : -1;
   };
-  int staged = next_selected(sel_lo - 1);
-  if (staged < 4) prefetch(staged);
+  const int first = win_tile ? 4 : next_sel(sel_lo - 1);  // 4: the window tile; -1: none
+  auto after = [&](int t) { return t == 4 ? next_sel(sel_lo - 1) : next_sel(t); };  // the tile after t
 
-  float lsum[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) lsum[i] = 0.0f;
-  uint32_t phase = 0;
+  bool ok = true;
   bool o_started = false;
-  const int hb = (warp >> 2) * 16;                  // this thread's 16 heads (of the CTA's 32)
-  const uint32_t key_row = (warp & 3) * 32 + lane;  // TMEM lane = key (softmax) / channel (epilogue)
-  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-
-  for (int it = 0; it < 5; ++it) {
-    // ---------------------------------------------------------------- the key tile
-    const bool win_turn = it == 0 && has_win;
-    const int t = win_turn ? 4 : staged;  // the window first, then the selected tiles in order
-    if (t == 4 && !win_turn) break;       // no selected tile left
-    if (t == 4) {
-      if (staged < 4) cp_async_wait_newest_pending();  // queries and window landed; records may still fly
-      else cp_async_wait_all();
-      if (kExt && a.rope_cos != nullptr) {
-        // q = q cos + rotate_half(q) sin on channels 448 + i / 480 + i (angle i), in place
-        __syncthreads();  // every thread's query pieces have landed
-        for (int p = tid; p < kHH * 32; p += kAttnThreads) {
-          const uint32_t h = static_cast<uint32_t>(p) >> 5, i = static_cast<uint32_t>(p) & 31u;
-          const float c = __ldg(a.rope_cos + qi * 32 + i), sn = __ldg(a.rope_sin + qi * 32 + i);
-          __nv_bfloat16* pa = reinterpret_cast<__nv_bfloat16*>(Qs + tile_off(h, 448u + i));
-          __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(Qs + tile_off(h, 480u + i));
-          const float x = __bfloat162float(*pa), y = __bfloat162float(*pb);
-          *pa = __float2bfloat16_rn(x * c - y * sn);
-          *pb = __float2bfloat16_rn(y * c + x * sn);
-        }
-      }
-      if (kExt && a.win_ring != nullptr) {
-        // FP8 window ring: row i of the tile is the entry of position newest - i, read
-        // after the wait on the previous kernel (the ring is written by an earlier call);
-        // E4M3 -> f16 in hardware, times the block's 2^e, -> bf16 (exact)
-        const int64_t newest = __ldg(a.win_start + qi);
-        const int32_t r = __ldg(a.req + qi);
-        const bool ring_ok = r >= 0 && r < a.win_ring_reqs && newest - wl + 1 >= 0;
-        if (!ring_ok && wl > 0 && tid == 0) report(a.err, CSA2_ERR_DEVICE, kInfoPos);
-#pragma unroll 2
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t task = static_cast<uint32_t>(tid + kAttnThreads * i);
-          const uint32_t row = (task & 7u) | (((task >> 5) & 15u) << 3);
-          const uint32_t j = ((task >> 3) & 3u) | ((task >> 9) << 2);
-          uint8_t* dst = Kt + tile_off(row, 32 * j);
-          if (!ring_ok || static_cast<int32_t>(row) >= wl) {  // no entry: zeros (masked)
+  uint32_t oph = 0;  // parity of the next O completion
+  const uint32_t idesc_s = idesc_f16(128, kHeads, 0, 0);
+  const uint32_t idesc_o = idesc_f16(128, kHeads, 1, 1);
+  // issuer c: S partial c over the channels of chunk c (called after the block barrier that
+  // follows the chunk's build)
+  auto issue_s = [&](int c) {
+    if (issuer && warp == c) {
+      const uint64_t dK0 = sdesc(smem_u32(Kt), 128, 8192), dQ0 = sdesc(smem_u32(Qs), 128, 8192);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + m * 128) = make_uint4(0, 0, 0, 0);
-            continue;
+      for (int k = 0; k < 8; ++k)
+        mma_f16(tmem + kSCol + 64u * c, dK0 + static_cast<uint64_t>(16 * (8 * c + k)),
+                dQ0 + static_cast<uint64_t>(16 * (8 * c + k)), idesc_s, k > 0 ? 1u : 0u);
+      mma_commit(s_bar);
+    }
+  };
+  // issuer c: O chunk c (called after the block barrier that follows the P stores)
+  auto issue_o = [&]() {
+    if (issuer) {
+      const uint32_t c = static_cast<uint32_t>(warp);
+      const uint64_t dV0 = sdesc(smem_u32(Kt), 8192, 128), dP0 = sdesc(smem_u32(Ps), 1024, 128);
+#pragma unroll
+      for (uint32_t kk = 0; kk < 8; ++kk)
+        mma_f16(tmem + 64u * c, dV0 + static_cast<uint64_t>(128u * c + 1024u * kk),
+                dP0 + static_cast<uint64_t>(128u * kk), idesc_o, (o_started || kk > 0) ? 1u : 0u);
+      mma_commit(&o_bar[c]);
+    }
+  };
+  {
+    // ================================================================ the tiles
+    // register prefetch of a selected tile: thread = (key 8 warp + lane % 8, 32-channel
+    // piece lane / 8 of each 128-channel chunk); per chunk 16 bytes of nibbles, 2 scale bytes
+    const uint32_t bkey = static_cast<uint32_t>(8 * warp + (lane & 7));
+    const uint32_t bj = static_cast<uint32_t>(lane >> 3);
+    uint4 pn[4];
+    uint32_t ps[4];
+    auto prefetch_chunk = [&](int ts, int c) {  // chunk c of selected tile ts (ts < 0 or 4: nothing)
+      const int32_t rid = (ts < 0 || ts == 4) ? -1 : recid[ts * 128 + static_cast<int>(bkey)];
+      if (rid >= 0) {
+        const uint8_t* rec = a.cache.kv + static_cast<int64_t>(rid) * kKvBytes;
+        pn[c] = __ldg(reinterpret_cast<const uint4*>(rec + 64 * c + 16 * bj));
+        ps[c] = __ldg(reinterpret_cast<const unsigned short*>(rec + 256 + 8 * c + 2 * bj));
+      } else {  // no entry: zeros (masked below)
+        pn[c] = make_uint4(0u, 0u, 0u, 0u);
+        ps[c] = 0u;
+      }
+    };
+    uint32_t dq[16];
+    auto dequant_chunk = [&](int c) {  // registers -> 32 f16 values of this thread's piece
+      const uint32_t sc2 = e4m3x2_f16x2_bits(ps[c]);
+      const uint32_t s0 = prmt(sc2, sc2, 0x1010u), s1 = prmt(sc2, sc2, 0x3232u);
+      const uint32_t wds[4] = {pn[c].x, pn[c].y, pn[c].z, pn[c].w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t o[4];
+        dequant8_f16(wds[m], m < 2 ? s0 : s1, o);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dq[4 * m + k] = o[k];
+      }
+    };
+    auto store_chunk = [&](int c) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<uint4*>(Kt + tile_off(bkey, 128u * c + 32u * bj + 8u * m)) =
+            make_uint4(dq[4 * m], dq[4 * m + 1], dq[4 * m + 2], dq[4 * m + 3]);
+    };
+    auto chunk_done = [&](int c) {  // chunk c is in place (and every S load is done): its S MMAs
+      fence_proxy_async_smem();
+      tc_fence_before();
+      cbar_sync();
+      tc_fence_after();
+      issue_s(c);
+    };
+
+    int cur = first;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) prefetch_chunk(cur == 4 ? after(4) : cur, c);
+    // ---- the first tile: the window (converted to f16 chunk by chunk) or a selected tile
+    if (cur == 4) {
+      if (!ring) {
+        cp_async_wait_all();
+        cbar_sync();  // every thread's window pieces have landed
+      }
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        if (!ring) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // 128 rows x 16 pieces of channels [128 c, 128 c + 128)
+            const uint32_t t = static_cast<uint32_t>(tid + kComputeThreads * i);
+            uint8_t* p = Kt + tile_off((t & 7u) | (((t >> 5) & 15u) << 3), 128u * c + 8u * (((t >> 3) & 3u) | ((t >> 9) << 2)));
+            *reinterpret_cast<uint4*>(p) = cvt16(*reinterpret_cast<const uint4*>(p));
           }
-          const int64_t pos = newest - row;
-          const uint8_t* rec = a.win_ring + (static_cast<int64_t>(r) * CSA2_WIN + pos % CSA2_WIN) * CSA2_WIN_BYTES;
-          const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(rec + 32 * j));
-          const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(rec + 32 * j + 16));
-          const float sc = ldexpf(1.0f, static_cast<int>(__ldg(rec + 512 + j)) - 127);
-          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        }
+        chunk_done(c);
+      }
+    } else if (cur >= 0) {
+      const int nx = after(cur);
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            uint32_t o[4];
+      for (int c = 0; c < 4; ++c) {
+        dequant_chunk(c);
+        prefetch_chunk(nx, c);  // the registers of chunk c are free again: the next tile's
+        store_chunk(c);
+        chunk_done(c);
+      }
+    }
+
+    float lsum[16];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 f = __half22float2(e4m3x2_f16x2((cw[2 * m + (k >> 1)] >> (16 * (k & 1))) & 0xFFFFu));
-              const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-              o[k] = *reinterpret_cast<const uint32_t*>(&bv);
-            }
-            *reinterpret_cast<uint4*>(dst + m * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int i = 0; i < 16; ++i) lsum[i] = 0.0f;
+    uint32_t sph = 0;
+    const uint32_t key = static_cast<uint32_t>(32 * qd + lane);  // softmax: TMEM lane = key
+    const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+    const int h0 = 16 * hg;
+
+    while (cur >= 0) {
+      // ---------------------------------------------------------------- S^T of tile cur
+      const bool w_ok = mbar_wait(s_bar, sph, abort);
+      sph ^= 1u;
+      if (cbar_or(!(ok && w_ok))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // ---------------------------------------------------------------- softmax
+      const bool kv_ok = cur == 4 ? static_cast<int32_t>(key) < wl : recid[cur * 128 + key] >= 0;
+      float x[16];
+      {  // the four partial sums, two at a time
+        uint32_t r[2][16];
+#pragma unroll
+        for (int p = 0; p < 4; p += 2) {
+          tmem_ld16(tmem + lane_base + kSCol + 64u * p + static_cast<uint32_t>(h0), r[0]);
+          tmem_ld16(tmem + lane_base + kSCol + 64u * (p + 1) + static_cast<uint32_t>(h0), r[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float v = __uint_as_float(r[0][i]) + __uint_as_float(r[1][i]);
+            x[i] = p == 0 ? v : x[i] + v;
           }
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = kv_ok ? x[i] * a.scale_log2 : -INFINITY;
       }
-    } else {
-      cp_async_wait_all();
-      __syncthreads();  // every thread's pieces of the staged records are visible
-      // item = (entry slot, 32-channel block j); a warp takes 8 slots x 4 blocks so that
-      // its 16-byte tile stores fill whole 128-byte lines
+      // the reference maxima live in shared memory (ref_s), read as broadcasts
+      bool need = false, rescale = false;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t task = static_cast<uint32_t>(tid + kAttnThreads * i);
-        const uint32_t slot = (task & 7u) | (((task >> 5) & 15u) << 3);
-        const uint32_t j = ((task >> 3) & 3u) | ((task >> 9) << 2);
-        const uint8_t* rec = Raw + slot * kKvBytes;
-        const uint4 nib = *reinterpret_cast<const uint4*>(rec + j * 16);
-        const uint32_t scw = *reinterpret_cast<const uint16_t*>(rec + 256 + j * 2);
-        const __nv_bfloat162 s0 = e4m3_bf16x2(scw & 0xFFu), s1 = e4m3_bf16x2(scw >> 8);
-        const uint32_t wds[4] = {nib.x, nib.y, nib.z, nib.w};
+      for (int i = 0; i < 16; ++i) need |= x[i] > ref_s[h0 + i] + kRescaleThreshold;
+      if (cbar_or(need)) {
+        // raise the reference maxima of the heads whose scores exceed them by 2^8
+        float* tmax = reinterpret_cast<float*>(Ps);  // [4][64] scratch: P is rewritten below
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          uint32_t o[4];
-          dequant8_bf16(wds[m], m < 2 ? s0 : s1, o);
-          *reinterpret_cast<uint4*>(Kt + tile_off(slot, 32 * j + 8 * m)) = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int i = 0; i < 16; ++i) {
+          const float m = redux_max(x[i]);
+          if (lane == i) tmax[qd * kHeads + h0 + i] = m;
+        }
+        cbar_sync();
+        bool ch = false;
+        if (tid < kHeads) {  // one thread per head decides (every reader of ref_s has passed the vote)
+          const float mt = fmaxf(fmaxf(tmax[tid], tmax[kHeads + tid]), fmaxf(tmax[2 * kHeads + tid], tmax[3 * kHeads + tid]));
+          const float old = ref_s[tid];
+          const float nw = (mt > old + kRescaleThreshold || (old == -INFINITY && mt != -INFINITY)) ? mt : old;
+          const float al = nw == old ? 1.0f : (old == -INFINITY ? 0.0f : exp2f(old - nw));
+          alpha[tid] = al;
+          ref_s[tid] = nw;
+          ch = al != 1.0f;
+        }
+        rescale = cbar_or(ch) && o_started;  // alpha and ref_s are visible
+#pragma unroll
+        for (int i = 0; i < 16; ++i) lsum[i] *= alpha[h0 + i];
+      }
+      // P = exp2(x - ref) -> f16, P^T tile (MN-major: 8 heads x 2 bytes per core row); the
+      // running sums add the rounded values, so that numerator and denominator agree
+      {
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const float p0 = x[i] == -INFINITY ? 0.0f : exp2f(x[i] - ref_s[h0 + i]);
+          const float p1 = x[i + 1] == -INFINITY ? 0.0f : exp2f(x[i + 1] - ref_s[h0 + i + 1]);
+          const __half2 ph = __floats2half2_rn(p0, p1);
+          const float2 pr = __half22float2(ph);
+          lsum[i] += pr.x;
+          lsum[i + 1] += pr.y;
+          pk[i / 2] = *reinterpret_cast<const uint32_t*>(&ph);
+        }
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t off = (key >> 3) * 1024u + static_cast<uint32_t>(2 * hg + g) * 128u + (key & 7u) * 16u;
+          *reinterpret_cast<uint4*>(Ps + off) = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
         }
       }
+      if (rescale) {
+        // O^T chunk hg, TMEM lanes of this quarter: every head column times its factor
+        // (after P, so that the scores' registers are free)
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t r[16];
+          const uint32_t addr = tmem + lane_base + static_cast<uint32_t>(64 * hg + 16 * q4);
+          tmem_ld16(addr, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha[16 * q4 + i]);
+          tmem_st16(addr, r);
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();  // the rescaled O^T columns (TMEM stores) before the O MMAs
+      cbar_sync();
+      tc_fence_after();
+      issue_o();
+      o_started = true;
+      // ---------------------------------------------------------------- the next tile
+      const int nt = after(cur);
+      if (nt < 0) break;
+      const int nx = after(nt);
+      // chunk c of the buffer is free once O chunk c has read it; the issuer runs the S MMAs
+      // of the chunks already in place while the later ones are built, and the records of
+      // the tile after next are loaded as each chunk's registers free up (unrolled: the
+      // prefetched registers are indexed by c)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        dequant_chunk(c);
+        prefetch_chunk(nx, c);
+        const bool c_ok = mbar_wait(&o_bar[c], oph, abort);
+        if (c_ok) store_chunk(c);
+        ok = ok && c_ok;
+        chunk_done(c);
+      }
+      oph ^= 1u;
+      cur = nt;
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (t != 4) {  // the staging buffer is free again: fetch the next selected tile
-      staged = next_selected(t);
-      if (staged < 4) prefetch(staged);
+    // the last tile's O chunks complete before the epilogue reads O^T
+    if (ok && o_started) {
+      bool w_ok = true;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) w_ok &= mbar_wait(&o_bar[c], oph, abort);
+      ok = ok && w_ok;
     }
-
-    // ---------------------------------------------------------------- S^T = K Q^T
-    // two issuing threads (warps 0 and 1): issuer i takes K-steps kk = i, i+2, ... into
-    // partial sums i and i + 2, so neither thread waits on the other's MMA latency
-    if (lane == 0 && warp < 2) {
-      const uint32_t me = static_cast<uint32_t>(warp);
-      const uint32_t kb = smem_u32(Kt), qb = smem_u32(Qs);
-#pragma unroll 4
-      for (uint32_t kk = me; kk < 32; kk += 2)
-        mma_bf16(tmem + kSCols + (kk & 3u) * kHH, sdesc(kb + kk * 256u, 128, 8192), sdesc(qb + kk * 256u, 128, 8192),
-                 idesc_s, kk >= 4 ? 1u : 0u);
-      mma_commit(&mma_bar[me]);
-      if (!mbar_wait(&mma_bar[me], phase, nullptr)) {
-        flags[0] = 1;
-        report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
+    if (!ok || *abort) {
+      ok = false;
+      *abort = 1;
+      if (tid == 0) report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
+      if (issuer) {  // every MMA this issuer started completes before TMEM is freed
+        mma_commit(drain);
+        mbar_wait(drain, 0, nullptr);
       }
     }
-    phase ^= 1;
-    __syncthreads();
-    tc_fence_after();
-    if (flags[0]) break;
-
-    // ---------------------------------------------------------------- softmax
-    const bool kv_ok = t == 4 ? static_cast<int32_t>(key_row) < wl : recoff[t * 128 + key_row] >= 0;
-    float x[16];
-    {
-      uint32_t r[16];
-      tmem_ld16(tmem + lane_base + kSCols + static_cast<uint32_t>(hb), r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(r[i]);
-#pragma unroll
-      for (uint32_t pp = 1; pp < 4; ++pp) {
-        tmem_ld16(tmem + lane_base + kSCols + pp * kHH + static_cast<uint32_t>(hb), r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] += __uint_as_float(r[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = kv_ok ? x[i] * a.scale_log2 : -INFINITY;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float m = redux_max(x[i]);
-      if (lane == i) tmax[(warp & 3) * kHH + hb + i] = m;
-    }
-    if (tid == 0) flags[1] = 0;
-    __syncthreads();
-    if (tid < kHH) {
-      const float mt = fmaxf(fmaxf(tmax[tid], tmax[kHH + tid]), fmaxf(tmax[2 * kHH + tid], tmax[3 * kHH + tid]));
-      const float old = ref[tid];
-      float nw = old;
-      if (mt > old + kRescaleThreshold || (old == -INFINITY && mt != -INFINITY)) nw = mt;
-      alpha[tid] = (old == -INFINITY) ? 0.0f : exp2f(old - nw);
-      ref[tid] = nw;
-      if (nw != old && old != -INFINITY) flags[1] = 1;
-    }
-    __syncthreads();
-    if (flags[1] && o_started) {
-      // rescale O^T columns (heads) and the running sums by alpha
-#pragma unroll
-      for (int i = 0; i < 16; ++i) lsum[i] *= alpha[hb + i];
-      for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
-        uint32_t r[32];
-        const uint32_t addr = tmem + lane_base + kOCols + static_cast<uint32_t>(c * kHH);
-        tmem_ld32(addr, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha[i]);
-        tmem_st32(addr, r);
-      }
-      tmem_st_wait();
-    }
-    // P = exp2(x - ref) -> bf16, P^T tile (MN-major: 8 heads x 2 bytes per core row)
-    {
-      uint32_t pk[8];
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const float r0 = ref[hb + i], r1 = ref[hb + i + 1];
-        const float p0 = (r0 == -INFINITY) ? 0.0f : exp2f(x[i] - r0);
-        const float p1 = (r1 == -INFINITY) ? 0.0f : exp2f(x[i + 1] - r1);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        lsum[i] += __low2float(pb);
-        lsum[i + 1] += __high2float(pb);
-        pk[i / 2] = *reinterpret_cast<const uint32_t*>(&pb);
-      }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t off = (key_row >> 3) * (kHH * 16u) + static_cast<uint32_t>((hb >> 3) + c) * 128u +
-                             (key_row & 7u) * 16u;
-        *reinterpret_cast<uint4*>(Ps + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---------------------------------------------------------------- O^T += V^T P^T
-    // issuer i accumulates output tiles 2i and 2i+1 (channels [256 i, 256 i + 256))
-    if (lane == 0 && warp < 2) {
-      const uint32_t me = static_cast<uint32_t>(warp);
-      const uint32_t kb = smem_u32(Kt), pb = smem_u32(Ps);
-      for (uint32_t kk = 0; kk < 8; ++kk) {
-#pragma unroll
-        for (uint32_t c = 2 * me; c < 2 * me + 2; ++c)
-          mma_bf16(tmem + kOCols + c * kHH, sdesc(kb + c * 2048u + kk * 16384u, 8192, 128),
-                   sdesc(pb + kk * (2u * kHH * 16u), kHH * 16u, 128), idesc_o, (o_started || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(&mma_bar[me]);
-      if (!mbar_wait(&mma_bar[me], phase, nullptr)) {
-        flags[0] = 1;
-        report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
-      }
-    }
-    phase ^= 1;
-    o_started = true;
-    __syncthreads();
-    tc_fence_after();
-    if (flags[0]) break;
-  }
-  cp_async_wait_all();  // no copy may land after the CTA is gone
-
-  // ---------------------------------------------------------------- epilogue
-  if (!flags[0]) {
-    // row sums: reduce the 128 key slots of each head
+    // ---- per-head sums over the 128 key lanes
+    float* lred = reinterpret_cast<float*>(Ps);  // [4][64]
+    cbar_sync();  // every warp is past its last P use
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       float v = lsum[i];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == i) lred[(warp & 3) * kHH + hb + i] = v;
+      if (lane == i) lred[qd * kHeads + h0 + i] = v;
     }
+  }
+  tc_fence_before();
+  __syncthreads();  // per-head sums are in place
+  tc_fence_after();
+  const bool have_o = !*abort && o_started;
+  if (tid < kHeads) {
+    const float l = lred_sum(reinterpret_cast<const float*>(Ps), tid);
+    ml[tid] = ref_s[tid];
+    ml[kHeads + tid] = have_o ? l : 0.0f;
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  const uint32_t d = static_cast<uint32_t>(128 * hg + 32 * qd + lane);  // output channel (O^T lane)
+  const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+  if (S == 1) {
     __syncthreads();
-    if (tid < kHH) {
-      const float l = lred[tid] + lred[kHH + tid] + lred[2 * kHH + tid] + lred[3 * kHH + tid];
+    if (tid < kHeads) {
+      const float l = ml[kHeads + tid], m = ml[tid];
       float lse2 = -INFINITY, inv = 0.0f;  // log2 sum-exp; O = O^T * inv
-      if (kSplit) {  // a partial over this CTA's tiles, merged by attn_combine_kernel
+      if (!kExt || a.sinks == nullptr) {
         if (l > 0.0f) {
-          lse2 = ref[tid] + log2f(l);
-          inv = 1.0f / l;
-        }
-        a.lpart[(qi * S + sp) * kHeads + h0 + tid] = lse2;
-      } else if (!kExt || a.sinks == nullptr) {
-        if (l > 0.0f) {
-          lse2 = ref[tid] + log2f(l);
+          lse2 = m + log2f(l);
           inv = 1.0f / l;
         }
       } else {
-        // the sink joins the denominator: O = O^T / (l + 2^(sink - ref)), taken relative
-        // to the larger of the two maxima so that nothing overflows
-        const float sk = __ldg(a.sinks + h0 + tid) * 1.4426950408889634f;
+        // the sink joins the denominator: O = O^T / (l + 2^(sink - ref)), taken relative to
+        // the larger of the two maxima so that nothing overflows
+        const float sk = __ldg(a.sinks + tid) * 1.4426950408889634f;
         if (l > 0.0f || sk != -INFINITY) {
-          const float m2 = l > 0.0f ? fmaxf(ref[tid], sk) : sk;
-          const float lt = (l > 0.0f ? l * exp2f(ref[tid] - m2) : 0.0f) + exp2f(sk - m2);
+          const float m2 = l > 0.0f ? fmaxf(m, sk) : sk;
+          const float lt = (l > 0.0f ? l * exp2f(m - m2) : 0.0f) + exp2f(sk - m2);
           lse2 = m2 + log2f(lt);
-          inv = l > 0.0f ? exp2f(ref[tid] - m2) / lt : 0.0f;
+          inv = l > 0.0f ? exp2f(m - m2) / lt : 0.0f;
         }
       }
-      if (a.lse && !kSplit) a.lse[qi * kHeads + h0 + tid] = lse2 * 0.6931471805599453f;
-      alpha[tid] = inv;  // reuse: the output scale per head
+      if (a.lse) a.lse[qi * kHeads + tid] = lse2 * 0.6931471805599453f;
+      alpha[tid] = inv;
     }
     __syncthreads();
-    // O^T (TMEM lane = channel, column = head) -> bf16 [32][512] staged in the free key
-    // tile, then written out with 16-byte coalesced stores
-    __nv_bfloat16* ostage = reinterpret_cast<__nv_bfloat16*>(Kt);
-    float* otail = reinterpret_cast<float*>(Ps);  // [32 heads][64] fp32 rotated channels (RoPE)
-    const bool rope = kExt && a.rope_cos != nullptr;
-    if (kSplit) {
-      // the normalised partial in fp32 [32][512], staged in the free key tile, then 16-byte
-      // coalesced stores
-      float* fstage = reinterpret_cast<float*>(Kt);
-      for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2; ++c) {
-        const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
+    // O^T (TMEM lane = channel, column = head) -> bf16 straight to the output: for each
+    // head a warp writes 32 consecutive channels (64 bytes)
+    __nv_bfloat16* og = a.out + qi * kHeads * CSA2_D;
+    float* otail = reinterpret_cast<float*>(Ps);  // [64 heads][64] fp32 rotated channels (RoPE)
+    {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
         uint32_t r[32];
-        if (o_started) {
-          tmem_ld32(tmem + lane_base + kOCols + static_cast<uint32_t>(c * kHH), r);
+        if (have_o) {
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(64 * hg + 32 * half), r);
           tmem_ld_wait();
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) fstage[i * CSA2_D + d] = o_started ? __uint_as_float(r[i]) * alpha[i] : 0.0f;
-      }
-      __syncthreads();
-      uint4* pg = reinterpret_cast<uint4*>(a.opart + ((qi * S + sp) * kHeads + h0) * CSA2_D);
-      const uint4* fs = reinterpret_cast<const uint4*>(fstage);
-      for (int i = tid; i < kHH * CSA2_D / 4; i += kAttnThreads) pg[i] = fs[i];
-    }
-    for (int c = (warp >> 2) * 2; c < (warp >> 2) * 2 + 2 && !kSplit; ++c) {
-      const uint32_t d = static_cast<uint32_t>(c) * 128u + key_row;
-      uint32_t r[32];
-      if (o_started) {
-        tmem_ld32(tmem + lane_base + kOCols + static_cast<uint32_t>(c * kHH), r);
-        tmem_ld_wait();
-      }
-      if (rope && d >= 448u) {  // rotated back below, in fp32
-#pragma unroll
-        for (int i = 0; i < 32; ++i) otail[i * 64 + (d - 448u)] = o_started ? __uint_as_float(r[i]) * alpha[i] : 0.0f;
-        continue;
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float o = o_started ? __uint_as_float(r[i]) * alpha[i] : 0.0f;
-        ostage[i * CSA2_D + d] = __float2bfloat16_rn(o);
+        for (int i = 0; i < 32; ++i) {
+          const int h = 32 * half + i;
+          const float o = have_o ? __uint_as_float(r[i]) * alpha[h] : 0.0f;
+          if (rope && d >= 448u)
+            otail[h * 64 + (d - 448u)] = o;
+          else
+            og[h * CSA2_D + d] = __float2bfloat16_rn(o);
+        }
       }
     }
     if (rope) {
       // o = o cos - rotate_half(o) sin: the rotation the values carried, undone at the
       // query's position
       __syncthreads();
-      for (int p = tid; p < kHH * 32; p += kAttnThreads) {
+      for (int p = tid; p < kHeads * 32; p += kAttnThreads) {
         const int h = p >> 5, i = p & 31;
         const float c = __ldg(a.rope_cos + qi * 32 + i), sn = __ldg(a.rope_sin + qi * 32 + i);
         const float x = otail[h * 64 + i], y = otail[h * 64 + 32 + i];
-        ostage[h * CSA2_D + 448 + i] = __float2bfloat16_rn(x * c + y * sn);
-        ostage[h * CSA2_D + 480 + i] = __float2bfloat16_rn(y * c - x * sn);
+        og[h * CSA2_D + 448 + i] = __float2bfloat16_rn(x * c + y * sn);
+        og[h * CSA2_D + 480 + i] = __float2bfloat16_rn(y * c - x * sn);
       }
     }
+  } else {
+    // ---- merge of the cluster's partials through L2: every CTA writes its raw O^T
+    // (relative to its own reference maxima) and its (max, sum) per head to the workspace;
+    // after one cluster barrier rank r combines heads [64 r / S, 64 (r + 1) / S).  Every CTA
+    // reaches the barrier, also after a failed wait (its partial then counts as empty).
+    float* opart = a.opart + static_cast<int64_t>(blockIdx.x) * kHeads * CSA2_D;  // [64][512]
+    float* mpart = a.mpart + static_cast<int64_t>(blockIdx.x) * 2 * kHeads;       // [2][64]
+    {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        if (have_o) {
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(64 * hg + 32 * half), r);
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) opart[(32 * half + i) * CSA2_D + d] = have_o ? __uint_as_float(r[i]) : 0.0f;
+      }
+    }
+    if (tid < kHeads) {
+      mpart[tid] = ml[tid];
+      mpart[kHeads + tid] = ml[kHeads + tid];
+    }
+    attn_cluster_sync();  // every partial of the cluster is written and visible
+    const int hlo = kHeads * sp / S, hhi = kHeads * (sp + 1) / S;
+    const float* opart0 = a.opart + static_cast<int64_t>(qi) * S * kHeads * CSA2_D;
+    const float* mpart0 = a.mpart + static_cast<int64_t>(qi) * S * 2 * kHeads;
+    float* fs = reinterpret_cast<float*>(Ps);  // [S][64] weight of each rank's partial
+    float* otail = fs + kAttnMaxSplits * kHeads;  // [owned heads][64] fp32 rotated channels (RoPE)
+    if (tid >= hlo && tid < hhi) {
+      float mr[kAttnMaxSplits], lr[kAttnMaxSplits];
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kAttnMaxSplits; ++r) {
+        mr[r] = r < S ? __ldcg(mpart0 + r * 2 * kHeads + tid) : -INFINITY;
+        lr[r] = r < S ? __ldcg(mpart0 + r * 2 * kHeads + kHeads + tid) : 0.0f;
+        if (lr[r] > 0.0f) M = fmaxf(M, mr[r]);
+      }
+      float sk = -INFINITY;
+      if (kExt && a.sinks != nullptr) sk = __ldg(a.sinks + tid) * 1.4426950408889634f;
+      const float M2 = fmaxf(M, sk);
+      float L = sk != -INFINITY ? exp2f(sk - M2) : 0.0f;
+#pragma unroll
+      for (int r = 0; r < kAttnMaxSplits; ++r)
+        if (lr[r] > 0.0f) L += lr[r] * exp2f(mr[r] - M2);
+#pragma unroll
+      for (int r = 0; r < kAttnMaxSplits; ++r)
+        if (r < S) fs[r * kHeads + tid] = (lr[r] > 0.0f && L > 0.0f) ? exp2f(mr[r] - M2) / L : 0.0f;
+      if (a.lse) a.lse[qi * kHeads + tid] = L > 0.0f ? (M2 + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
     __syncthreads();
-    uint4* og = reinterpret_cast<uint4*>(a.out + (qi * kHeads + h0) * CSA2_D);
-    const uint4* os = reinterpret_cast<const uint4*>(ostage);
-    for (int i = tid; i < kHH * CSA2_D / 8 && !kSplit; i += kAttnThreads) og[i] = os[i];
-  }
-  // drain outstanding MMAs, then free TMEM
-  if (lane == 0 && warp < 2) {
-    mma_commit(&drain[warp]);
-    mbar_wait(&drain[warp], 0, nullptr);
+    // items of 4 channels of one owned head: the S partials with 16-byte loads, weighted,
+    // -> bf16 (with RoPE the last 64 channels go through otail and are rotated below).  A
+    // thread's items are at most 8 (32 heads x 128 groups / 512 threads); all of their loads
+    // are issued before the first is used.
+    const int items = (hhi - hlo) * (CSA2_D / 4);
+    float4 accs[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) accs[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < S; ++r) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int it = tid + kComputeThreads * k;
+        const int h = hlo + it / (CSA2_D / 4), g = it % (CSA2_D / 4);
+        v[k] = it < items ? __ldcg(reinterpret_cast<const float4*>(opart0 + (static_cast<int64_t>(r) * kHeads + h) * CSA2_D) + g)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int it = tid + kComputeThreads * k;
+        const int h = hlo + (it < items ? it / (CSA2_D / 4) : 0);
+        const float f = fs[r * kHeads + h];
+        accs[k].x += f * v[k].x;
+        accs[k].y += f * v[k].y;
+        accs[k].z += f * v[k].z;
+        accs[k].w += f * v[k].w;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int it = tid + kComputeThreads * k;
+      if (it >= items) break;
+      const int h = hlo + it / (CSA2_D / 4), g = it % (CSA2_D / 4);
+      const float4 acc = accs[k];
+      if (rope && g >= 112) {
+        float* t = otail + (h - hlo) * 64 + (4 * g - 448);
+        t[0] = acc.x;
+        t[1] = acc.y;
+        t[2] = acc.z;
+        t[3] = acc.w;
+      } else {
+        const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(a.out + (qi * kHeads + h) * CSA2_D + 4 * g) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+      }
+    }
+    if (rope) {
+      __syncthreads();
+      for (int p = tid; p < (hhi - hlo) * 32; p += kAttnThreads) {
+        const int hh = p >> 5, i = p & 31;
+        const float c = __ldg(a.rope_cos + qi * 32 + i), sn = __ldg(a.rope_sin + qi * 32 + i);
+        const float x = otail[hh * 64 + i], y = otail[hh * 64 + 32 + i];
+        __nv_bfloat16* dst = a.out + (qi * kHeads + hlo + hh) * CSA2_D;
+        dst[448 + i] = __float2bfloat16_rn(x * c + y * sn);
+        dst[480 + i] = __float2bfloat16_rn(y * c - x * sn);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -526,80 +729,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-size_t attn_smem_bytes() {
-  return 1024 + kKtBytes + kQsBytes + kPsBytes + kRawBytes + (2 + 8) * kHH * sizeof(float) + CSA2_TOPK * 8 + 16 +
-         4 * sizeof(uint64_t) + 16;
-}
+size_t attn_smem_bytes() { return kAttnSmem; }
 
-// Merge of the key-tile splits: one warp per (query, head).  The total log2 sum-exp is
-// L = log2(sum_s 2^L_s) and O = sum_s 2^(L_s - L) O_s (each O_s already normalised by
-// its own sum); lanes take 16 channels each.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
-  pdl_trigger();
-  pdl_wait();  // the partials come from the attention kernel
-  const int lane = threadIdx.x & 31;
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (item >= a.n_q * kHeads) return;
-  const int64_t qi = item / kHeads;
-  const int h = static_cast<int>(item % kHeads);
-  const int S = a.splits;
-  float ls[kAttnMaxSplits];
-  float m = -INFINITY;
-#pragma unroll
-  for (int s = 0; s < kAttnMaxSplits; ++s) {
-    ls[s] = s < S ? __ldg(a.lpart + (qi * S + s) * kHeads + h) : -INFINITY;
-    m = fmaxf(m, ls[s]);
-  }
-  float tot = 0.0f;
-#pragma unroll
-  for (int s = 0; s < kAttnMaxSplits; ++s) tot += ls[s] == -INFINITY ? 0.0f : exp2f(ls[s] - m);
-  const float lse2 = m == -INFINITY ? -INFINITY : m + log2f(tot);
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-#pragma unroll
-  for (int s = 0; s < kAttnMaxSplits; ++s) {
-    if (ls[s] == -INFINITY) continue;
-    const float wgt = exp2f(ls[s] - lse2);
-    const float4* src = reinterpret_cast<const float4*>(a.opart + ((qi * S + s) * kHeads + h) * CSA2_D + 16 * lane);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 v = __ldg(src + k);
-      acc[4 * k + 0] += wgt * v.x;
-      acc[4 * k + 1] += wgt * v.y;
-      acc[4 * k + 2] += wgt * v.z;
-      acc[4 * k + 3] += wgt * v.w;
+// Splits per query for this launch: the most (up to the 5 tiles) that keep every CTA of a
+// batch in one wave, reduced while the device cannot hold a cluster of that size with this
+// kernel's shared memory (queried once per device and size).
+int attn_splits_for(int64_t n_q, int sm_count, bool ext) {
+  static std::atomic<int> fits[2][kMaxDevices][kAttnMaxSplits + 1];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int S = attn_wave_splits(n_q, sm_count);
+  for (; S > 1; --S) {
+    int v = (dev >= 0 && dev < kMaxDevices) ? fits[ext][dev][S].load(std::memory_order_relaxed) : 0;
+    if (v == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(S), 1, 1);
+      cfg.blockDim = dim3(kAttnThreads, 1, 1);
+      cfg.dynamicSmemBytes = kAttnSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n_act = 0;
+      auto* kernel = ext ? attn_kernel<true> : attn_kernel<false>;
+      static std::atomic<int> limit_set[2][kMaxDevices];
+      cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kernel), kAttnSmem, limit_set[ext]);
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n_act, kernel, &cfg);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        n_act = 0;
+      }
+      v = n_act > 0 ? 1 : -1;
+      if (dev >= 0 && dev < kMaxDevices) fits[ext][dev][S].store(v, std::memory_order_relaxed);
     }
+    if (v > 0) break;
   }
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-    o[i] = *reinterpret_cast<const uint32_t*>(&b);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(a.out + (qi * kHeads + h) * CSA2_D + 16 * lane);
-  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-  if (lane == 0 && a.lse) a.lse[qi * kHeads + h] = lse2 * 0.6931471805599453f;
+  return S;
 }
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_q == 0) return cudaSuccess;
-  const size_t smem = attn_smem_bytes();
-  static std::atomic<int> limit_set[3][kMaxDevices];
+  static std::atomic<int> limit_set[2][kMaxDevices];
   const bool ext = a.sinks != nullptr || a.rope_cos != nullptr || a.win_ring != nullptr;
-  const int S = ext ? 1 : a.splits;
-  auto* kernel = ext ? attn_kernel<true, false> : (S > 1 ? attn_kernel<false, true> : attn_kernel<false, false>);
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kernel), smem, limit_set[ext ? 2 : (S > 1 ? 1 : 0)]);
+  auto* kernel = ext ? attn_kernel<true> : attn_kernel<false>;
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kernel), kAttnSmem, limit_set[ext ? 1 : 0]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kernel, dim3(static_cast<unsigned>(2 * a.n_q * S)), dim3(kAttnThreads), smem, stream, nullptr,
-                    a);
-}
-
-cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream) {
-  if (a.n_q == 0) return cudaSuccess;
-  const int64_t blocks = (a.n_q * kHeads + 7) / 8;
-  return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, nullptr, a);
+  const int S = a.splits;
+  cudaLaunchAttribute cl;
+  cl.id = cudaLaunchAttributeClusterDimension;
+  cl.val.clusterDim.x = static_cast<unsigned>(S);
+  cl.val.clusterDim.y = 1;
+  cl.val.clusterDim.z = 1;
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(a.n_q * S)), dim3(kAttnThreads), kAttnSmem, stream,
+                    S > 1 ? &cl : nullptr, a);
 }
 
 }  // namespace csa2

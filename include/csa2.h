@@ -319,6 +319,19 @@ csa2_status csa2_sparse_attn_reuse(const csa2_step* step, void* ws, size_t ws_by
  * 6 candidate pool). */
 csa2_status csa2_check(void* ws, csa2_stream_t stream, int32_t* info);
 
+/* Tensor-core throughput probe (a measurement utility; the pages have no counterpart):
+ * n_ctas CTAs (one per SM when n_ctas is the SM count) each run `iters` back-to-back
+ * tcgen05.mma of M = 128 and the given N, issued by `issuers` threads into separate TMEM
+ * accumulators, with zeroed shared-memory operands; cycles[i] (device, int64) receives CTA
+ * i's clock cycles from the first issue to the completion of the last MMA.
+ *   kind 0: kind::f16, f16 x f16 -> fp32, K = 16 per MMA
+ *   kind 1: kind::mxf4nvf4 scale_vec::4X (E2M1 x E2M1, E4M3 scale per 16), K = 64
+ * FLOPs per MMA = 2 * 128 * n * K.  n in {64, 128, 256}; issuers in 1..4 with
+ * issuers * n <= 448; iters in [1, 2^22].  "A Precision Primer" of "DeepSeek's Attention
+ * and KV Cache" quotes the FP4 rate as a multiple of bf16 on Blackwell; this measures it. */
+csa2_status csa2_probe_mma(int32_t kind, int32_t n, int32_t iters, int32_t issuers, int32_t n_ctas, int64_t* cycles,
+                           csa2_stream_t stream);
+
 /* Number of kernels this library has launched in this process. */
 int64_t csa2_launch_count(void);
 

@@ -1,5 +1,6 @@
 """Sparse + window MQA parity (Reuse mode, given indices): bf16 output within 2e-2
-max-abs of the fp64 oracle ("DeepSeek's Attention and KV Cache", "DeepSeek-V4": 512
+max-abs of the fp64 oracle beyond the bf16 rounding of the exact output (half an ulp of
+it; "DeepSeek's Attention and KV Cache", "DeepSeek-V4": 512
 selected entries concatenated with the 128 window entries, one shared vector as key and
 value; "From MLA to DSA to HCA/CSA", "What replaced MLA": K and V are the same tensor)."""
 import numpy as np
@@ -8,17 +9,18 @@ import torch
 
 import synth
 from helpers import Cache, dev, dev_bf16, fill_cache
+from test_gpu_fullsize import attn_excess
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
 
 
 def _reuse(orc, csa2, n_entries, idx, req_q, win_len, seed, qscale=1.0, win_rows=None, sinks=None, rope=None,
-           win_start=None):
+           win_start=None, outliers=0.0):
     n_req = len(n_entries)
     max_pages = (max(n_entries) + 127) // 128
     cache = Cache(n_req, max_pages)
-    lat, key, req_e, pos_e = fill_cache(cache, n_entries, seed)
+    lat, key, req_e, pos_e = fill_cache(cache, n_entries, seed, outlier_frac=outliers)
     kv_h, ix_h = orc.alloc_pages(cache.n_pages)
     orc.pack_kv(lat, key, req_e, pos_e, kv_h, ix_h, None, max_pages)
     n_q = len(req_q)
@@ -60,7 +62,7 @@ def _reuse(orc, csa2, n_entries, idx, req_q, win_len, seed, qscale=1.0, win_rows
                                            window[ws_:ws_ + max(1, win_len[i])], int(win_len[i]), None,
                                            None if sinks is None else np.asarray(sinks, np.float32),
                                            rc, rs, None, max_pages)
-        err = np.abs(O[i] - Oref).max()
+        err = attn_excess(O[i], Oref)
         assert err <= TOL, (i, err)
         fin = np.isfinite(lref)
         assert np.array_equal(fin, np.isfinite(L[i]))
@@ -102,17 +104,30 @@ def test_attn_shared_window_rows_prefill_style(orc, csa2):
     _reuse(orc, csa2, n, idx, [0] * n_q, [128, 128, 128], seed=53, win_rows=130)
 
 
-def test_attn_sinks_and_partial_rope(orc, csa2):
+@pytest.mark.parametrize("n_q", [3, 80])
+def test_attn_sinks_and_partial_rope(orc, csa2, n_q):
     """Per-head sinks join the softmax; the query's trailing 64 channels are rotated at
     its position and the output rotated back ("From MLA to DSA to HCA/CSA", "The sliding
-    window" and "What replaced MLA")."""
+    window" and "What replaced MLA").  3 queries take the cluster merge (5 CTAs each), 80
+    one CTA each."""
     n = [1800]
-    n_q = 3
     idx = np.stack([synth.distinct_indices(20 + i, 1800, 512) for i in range(n_q)])
+    idx[-1, 100:] = -1                   # a short selection
     sinks = 2.0 * synth.normal_f32(21, (64,))
     sinks[:4] = [-30.0, 0.0, 8.0, 30.0]  # negligible, even, dominant, overwhelming
     rope = synth.rng(22).uniform(-np.pi, np.pi, (n_q, 32))
-    _reuse(orc, csa2, n, idx, [0] * n_q, [128, 77, 0], seed=54, qscale=2.0, sinks=sinks, rope=rope)
+    wl = [[128, 77, 0][i % 3] for i in range(n_q)]
+    _reuse(orc, csa2, n, idx, [0] * n_q, wl, seed=54, qscale=2.0, sinks=sinks, rope=rope)
+
+
+@pytest.mark.parametrize("n_q", [2, 90])
+def test_attn_outlier_entries_peaky(orc, csa2, n_q):
+    """5 % of the entries x 8 (large E4M3 block scales) and peaky queries (Q x 8): outputs
+    reach |O| of several units, where the bf16 output rounding itself is a visible part
+    of the error; the bound stays 2e-2 beyond half an ulp of the exact output."""
+    n = [3000]
+    idx = np.stack([synth.distinct_indices(90 + i, 3000, 512) for i in range(n_q)])
+    _reuse(orc, csa2, n, idx, [0] * n_q, [128] * n_q, seed=59, qscale=8.0, outliers=0.05)
 
 
 def test_attn_rope_only_and_sinks_only(orc, csa2):
@@ -137,12 +152,13 @@ def test_attn_bounded_replay_window(orc, csa2):
     _reuse(orc, csa2, n, idx, [0] * len(pos), lens, seed=57, win_rows=301 + base, win_start=starts)
 
 
-@pytest.mark.parametrize("n_q", [17, 22, 30])
+@pytest.mark.parametrize("n_q", [3, 34, 45, 60, 80])
 def test_attn_key_tile_splits(orc, csa2, n_q):
-    """Small batches split each query's key tiles over several CTAs and merge the partial
-    outputs by their sums of exponentials; on 152 SMs these batch sizes take 4, 3 and 2
-    splits (smaller batches take 5).  Rows mix full selections, short selections (empty
-    tiles in some splits), window-only rows and rows with no key at all."""
+    """Batches smaller than the SM count split each query's key tiles over a cluster of CTAs
+    that merge their partial outputs by their sums of exponentials through distributed
+    shared memory; on 152 SMs these batch sizes take 5, 4, 3, 2 and 1 CTAs per query.  Rows
+    mix full selections, short selections (empty tiles in some splits), window-only rows
+    and rows with no key at all."""
     n = [700, 300]
     pats = []
     for i in range(n_q):

@@ -8,7 +8,8 @@ and the new entries.  Checked there: packed bytes bit-exact (whole pages of the 
 main-KV records of the selected entries), index scores within 1e-3 * M on the windows
 ("DeepSeek's Attention and KV Cache", "DeepSeek-V3.2" indexer; "From MLA to DSA to
 HCA/CSA", "CSA" scorer), the top-512 bit-exact on the GPU's own score row, attention
-within 2e-2 max-abs and lse within 1e-2 on the GPU-selected indices ("DeepSeek-V4":
+within 2e-2 max-abs beyond the bf16 output rounding (half an ulp of the exact value) and
+lse within 1e-2 on the GPU-selected indices ("DeepSeek-V4":
 selected entries plus the 128-row window).  One full 131072-entry row also reports the
 overlap of the GPU's selection with the oracle's own top-512."""
 import numpy as np
@@ -73,16 +74,19 @@ def oracle_request(orc, dc, r, n_cached, positions, new_lat=None, new_key=None, 
     return kv_h, ix_h
 
 
-def attn_tol(orc, kv_h, sel, win_rows, Oref, max_pages, outliers):
-    """2e-2 max-abs; with x8 outlier entries the bf16 rounding of the probabilities and of
-    the output alone allows 2^-9 (2 max|v| + max|O|) (v: the attended values), so the
-    larger of the two applies there."""
-    if not outliers:
-        return TOL
-    vmax = float(np.abs(synth.bf16_to_f32(win_rows)).max())
-    for e in sel[sel >= 0]:
-        vmax = max(vmax, float(np.abs(orc.read_main(kv_h, 0, int(e), None, max_pages)).max()))
-    return max(TOL, 2.0 ** -9 * (2.0 * vmax + float(np.abs(Oref).max())))
+def bf16_half_ulp(x):
+    """Half a unit in the last place of bf16 (8 significant bits) at |x|: the rounding of an
+    exact output to the bf16 output format alone can be off by this much."""
+    ax = np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(ax)).astype(np.int64) - 8)
+
+
+def attn_excess(O, Oref):
+    """max over elements of |O - Oref| - half_ulp_bf16(Oref): must stay within 2e-2.  The
+    bound is the stated 2e-2 max-abs plus the rounding the bf16 output format itself
+    imposes (half an ulp of the exact value, 0.0625 at |O| in [16, 32), where the x8
+    outlier layers put some outputs); nothing in it depends on how the kernel computes."""
+    return float((np.abs(O - Oref) - bf16_half_ulp(Oref)).max())
 
 
 def check_request(orc, csa2, dc, r, *, n_cached, nv, S_row, sel, q, q_idx, w, win_rows, O, L, windows,
@@ -106,10 +110,10 @@ def check_request(orc, csa2, dc, r, *, n_cached, nv, S_row, sel, q, q_idx, w, wi
         assert np.array_equal(kv_g[off:off + KVB], kv_h[off:off + KVB]), (r, e)
     assert np.array_equal(sel, orc.topk(S_row[:nv], 512)), r
     Oref, lref = orc.attention(q, sel, kv_h, 0, win_rows, len(win_rows), None, None, dc.max_pages)
-    err = np.abs(O - Oref).max()
-    tol = attn_tol(orc, kv_h, sel, win_rows, Oref, dc.max_pages, dc.frac > 0)
-    print(f"request {r}: attention max-abs error {err:.4f} (tolerance {tol:.4f})")
-    assert err <= tol, (r, err, tol)
+    err, exc = float(np.abs(O - Oref).max()), attn_excess(O, Oref)
+    print(f"request {r}: attention max-abs error {err:.4f}, beyond the bf16 output rounding {exc:.4f} "
+          f"(max |O| {float(np.abs(Oref).max()):.2f})")
+    assert exc <= TOL, (r, err, exc)
     assert np.abs(L - lref).max() <= 1e-2, r
 
 
@@ -206,7 +210,7 @@ def test_reuse_and_reindex_128x262144(orc, csa2):
     for r in (0, 101):
         kv_h, _ = oracle_request(orc, dc, r, T, selh[r])
         Oref, lref = orc.attention(qh[r], selh[r], kv_h, 0, rw[128 * r:128 * r + 128], 128, None, None, mp)
-        assert np.abs(O[r] - Oref).max() <= TOL, r
+        assert attn_excess(O[r], Oref) <= TOL, r
         assert np.abs(L[r] - lref).max() <= 1e-2, r
     # Reindex: the shared packed keys rescored by a fresh indexer query
     q_idx = synth.torch_normal_bf16(520603, (B, 64, 128), "cuda")

@@ -1,8 +1,9 @@
 """A whole layer step captured in a CUDA graph: the C ABI launches only on the caller's
 stream and neither allocates nor synchronises inside a step, so the Full-mode step
-(pack, indexer, top-k, attention — chained by programmatic dependent launch, with the
-split attention's combine at this batch size) can be captured after one eager call and
-replayed; the replays reproduce the eager outputs bit for bit."""
+(pack, indexer, top-k, attention — chained by programmatic dependent launch; at this
+batch size the attention runs as clusters of key splits merged through the workspace)
+can be captured after one eager call and replayed; the replays reproduce the eager
+outputs bit for bit."""
 import numpy as np
 import pytest
 import torch
