@@ -72,6 +72,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(const TopkArgs 
 // a warp with shuffles, then over the 16 warp totals in warp 0.
 __device__ void threshold_bin(const uint32_t* h, uint32_t k, int* s_bin, uint32_t* s_above, uint32_t* s_warp) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) {  // defaults when no bin reaches k (a histogram of fewer than k keys)
+    *s_bin = 0;
+    *s_above = 0;
+  }
   const uint32_t loc = h[4 * t] + h[4 * t + 1] + h[4 * t + 2] + h[4 * t + 3];
   uint32_t x = loc;  // inclusive suffix within the warp
 #pragma unroll
@@ -612,6 +616,10 @@ __device__ bool select_candidates(const uint2* cand, uint32_t nc, uint32_t need,
       const bool in = threadIdx.x + j * kTopkThreads < nc && (sh + 8 >= 32 || (d >> (sh + 8)) == prefix);
       if (in) atomicAdd(&hc[(d >> sh) & 255u], 1u);
     }
+    if (threadIdx.x == 0) {  // defaults when no digit reaches need_l (inconsistent counts)
+      s_digit = 0;
+      s_above = 0;
+    }
     __syncthreads();
     if (threadIdx.x < 32) {
       // lane l owns digits 8l .. 8l+7; counts from the top of the range
@@ -647,15 +655,17 @@ __device__ bool select_candidates(const uint2* cand, uint32_t nc, uint32_t need,
   const uint32_t start = *n_picked;
   if (threadIdx.x == 0) *n_ties_ctr = 0;
   __syncthreads();
+  // appends with one shared atomic per warp and list (a per-thread atomic on one counter
+  // serialises hundreds of updates)
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const uint32_t i = threadIdx.x + j * kTopkThreads;
-    if (i < nc && key[j] > vstar) {
-      sel[atomicAdd(n_picked, 1u)] = static_cast<int32_t>(cand[i].y);
-    } else if (i < nc && key[j] == vstar) {
-      const uint32_t tslot = atomicAdd(n_ties_ctr, 1u);
-      if (tslot < static_cast<uint32_t>(kBins)) ties[tslot] = static_cast<int32_t>(cand[i].y);
-    }
+    const bool hi = i < nc && key[j] > vstar, eq = i < nc && key[j] == vstar;
+    uint32_t slot = 0;
+    append(n_picked, hi, slot);
+    if (hi && slot < static_cast<uint32_t>(CSA2_TOPK)) sel[slot] = static_cast<int32_t>(cand[i].y);
+    append(n_ties_ctr, eq, slot);
+    if (eq && slot < static_cast<uint32_t>(kBins)) ties[slot] = static_cast<int32_t>(cand[i].y);
   }
   __syncthreads();
   const uint32_t n_ties = *n_ties_ctr;
@@ -669,7 +679,9 @@ __device__ bool select_candidates(const uint2* cand, uint32_t nc, uint32_t need,
     bitonic_sort(ties, p2);
   }
   const uint32_t taken = start + (need - need_l);  // keys above v*
-  for (uint32_t i = threadIdx.x; i < need_l; i += kTopkThreads) sel[taken + i] = ties[i];
+  const uint32_t n_take = need_l < n_ties ? need_l : n_ties;
+  for (uint32_t i = threadIdx.x; i < n_take; i += kTopkThreads)
+    if (taken + i < static_cast<uint32_t>(CSA2_TOPK)) sel[taken + i] = ties[i];
   __syncthreads();
   if (threadIdx.x == 0) *n_picked = start + need;
   __syncthreads();
@@ -825,42 +837,54 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
   const float* row = a.scores + q * a.ld;
   uint32_t* hl = h + (threadIdx.x & 1) * kBins;  // two copies halve the atomic contention on busy bins
   // ---- pass 1: histogram of the top 11 key bits of every key, or of every block maximum
-  for (int64_t base = c0; base < c1; base += 16 * kTopkThreads) {
-    float4 v[4];
+  // (8 float4 per thread per round, all loads issued before the first is used; offsets
+  // relative to the chunk in 32 bits, and full rounds without per-element bounds checks)
+  {
+    const int32_t len = c1 > c0 ? static_cast<int32_t>(c1 - c0) : 0;
+    const float* crow = row + c0;
+    for (int32_t base = 0; base < len; base += 32 * kTopkThreads) {
+      float4 v[8];
+      const bool full = base + 32 * kTopkThreads <= len;
+      if (full) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
-      if (i0 + 3 < c1) {
-        v[u] = __ldg(reinterpret_cast<const float4*>(row + i0));
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(reinterpret_cast<const float4*>(crow + base) + u * kTopkThreads + threadIdx.x);
       } else {
-        v[u].x = i0 + 0 < c1 ? __ldg(row + i0 + 0) : NAN;
-        v[u].y = i0 + 1 < c1 ? __ldg(row + i0 + 1) : NAN;
-        v[u].z = i0 + 2 < c1 ? __ldg(row + i0 + 2) : NAN;
-        v[u].w = i0 + 3 < c1 ? __ldg(row + i0 + 3) : NAN;
-      }
-    }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i0 = base + (static_cast<int64_t>(u) * kTopkThreads + threadIdx.x) * 4;
-      if (by_blocks) {
-        // lanes 8g .. 8g + 7 hold the 32 entries of one block
-        uint32_t m = 0;
-        m = max(m, i0 + 0 < c1 ? order_key(v[u].x) : 0u);
-        m = max(m, i0 + 1 < c1 ? order_key(v[u].y) : 0u);
-        m = max(m, i0 + 2 < c1 ? order_key(v[u].z) : 0u);
-        m = max(m, i0 + 3 < c1 ? order_key(v[u].w) : 0u);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        if ((lane & 7u) == 0 && i0 < c1) {
-          bm[(i0 - c0) >> 5] = m;
-          atomicAdd(&hl[m >> 21], 1u);
+        for (int u = 0; u < 8; ++u) {
+          const int32_t i0 = base + (u * kTopkThreads + static_cast<int32_t>(threadIdx.x)) * 4;
+          if (i0 + 3 < len) {
+            v[u] = __ldg(reinterpret_cast<const float4*>(crow + i0));
+          } else {
+            v[u].x = i0 + 0 < len ? __ldg(crow + i0 + 0) : NAN;
+            v[u].y = i0 + 1 < len ? __ldg(crow + i0 + 1) : NAN;
+            v[u].z = i0 + 2 < len ? __ldg(crow + i0 + 2) : NAN;
+            v[u].w = i0 + 3 < len ? __ldg(crow + i0 + 3) : NAN;
+          }
         }
-      } else {
-        if (i0 + 0 < c1) atomicAdd(&hl[order_key(v[u].x) >> 21], 1u);
-        if (i0 + 1 < c1) atomicAdd(&hl[order_key(v[u].y) >> 21], 1u);
-        if (i0 + 2 < c1) atomicAdd(&hl[order_key(v[u].z) >> 21], 1u);
-        if (i0 + 3 < c1) atomicAdd(&hl[order_key(v[u].w) >> 21], 1u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int32_t i0 = base + (u * kTopkThreads + static_cast<int32_t>(threadIdx.x)) * 4;
+        const uint32_t k0 = full || i0 + 0 < len ? order_key(v[u].x) : 0u;
+        const uint32_t k1 = full || i0 + 1 < len ? order_key(v[u].y) : 0u;
+        const uint32_t k2 = full || i0 + 2 < len ? order_key(v[u].z) : 0u;
+        const uint32_t k3 = full || i0 + 3 < len ? order_key(v[u].w) : 0u;
+        if (by_blocks) {
+          // lanes 8g .. 8g + 7 hold the 32 entries of one block
+          uint32_t m = max(max(k0, k1), max(k2, k3));
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          if ((lane & 7u) == 0 && i0 < len) {
+            bm[i0 >> 5] = m;
+            atomicAdd(&h[m >> 21], 1u);
+          }
+        } else {
+          if (full || i0 + 0 < len) atomicAdd(&hl[k0 >> 21], 1u);
+          if (full || i0 + 1 < len) atomicAdd(&hl[k1 >> 21], 1u);
+          if (full || i0 + 2 < len) atomicAdd(&hl[k2 >> 21], 1u);
+          if (full || i0 + 3 < len) atomicAdd(&hl[k3 >> 21], 1u);
+        }
       }
     }
   }
@@ -897,7 +921,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
     }
     __syncthreads();
     const uint32_t nbl = lctr[2] < static_cast<uint32_t>(kBins) ? lctr[2] : static_cast<uint32_t>(kBins);
-    gather_block_candidates<4>(row, c0, c1, blist, nbl, bstar, lcand, kClLocalCap, &lctr[1]);
+    gather_block_candidates<6>(row, c0, c1, blist, nbl, bstar, lcand, kClLocalCap, &lctr[1]);
   } else {
     // ---- pass 2 (keys): stage this chunk's entries above / in the threshold bin (the
     // chunk is mostly still in L2)
@@ -978,11 +1002,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_cluster_kernel(const Top
                              &ctr[2], &lctr[3]);
   }
   if (!done) full_row_select(a, q, nv, h, s_warp, sel, &ctr[2]);
-  // ascending output: a bitmap of the row in the free candidate buffer when it fits
-  if (nv <= static_cast<int64_t>(kClCandCap) * 2 * 32)
-    bitmap_indices_out(sel, a.k, nv, reinterpret_cast<uint32_t*>(cand), s_warp, out);
-  else
-    sort_indices_out(threadIdx.x < a.k ? sel[threadIdx.x] : INT_MAX, reinterpret_cast<int32_t*>(hsum), out, a.k);
+  // ascending output: a shuffle sort per warp, then each index's rank from binary searches
+  // in the 16 sorted runs (one block barrier)
+  __syncthreads();
+  sort_indices_out(threadIdx.x < a.k ? sel[threadIdx.x] : INT_MAX, reinterpret_cast<int32_t*>(hsum), out, a.k);
 }
 
 size_t topk_cluster_smem() {
