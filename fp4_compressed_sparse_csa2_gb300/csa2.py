@@ -73,6 +73,8 @@ def _load():
         getattr(L, f).argtypes = [ctypes.POINTER(csa2_step), vp, sz, vp]
     L.csa2_topk_noalloc.argtypes = [vp, i64, vp, i64, i64, i32, vp, vp]
     L.csa2_topk_noalloc.restype = ctypes.c_int
+    L.csa2_debug_set_wait_limit.argtypes = [ctypes.c_uint64]
+    L.csa2_debug_set_wait_limit.restype = ctypes.c_int
     L.csa2_probe_mma.argtypes = [i32, i32, i32, i32, i32, vp, vp]
     L.csa2_probe_mma.restype = ctypes.c_int
     L.csa2_topk_noalloc_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
@@ -202,6 +204,11 @@ def probe_mma(kind: int, n: int, iters: int, issuers: int, n_ctas: int, cycles, 
     """Tensor-core throughput probe: cycles (int64 [n_ctas], device) per CTA for `iters` MMAs
     of M = 128 and the given N per issuer (kind 0 f16, 1 NVFP4)."""
     _check(lib.csa2_probe_mma(int(kind), int(n), int(iters), int(issuers), int(n_ctas), _ptr(cycles), _stream(stream)))
+
+
+def debug_set_wait_limit(ns: int):
+    """Bound (ns) of the pipeline waits of kernels launched afterwards; 0 = the default 2 s."""
+    _check(lib.csa2_debug_set_wait_limit(int(ns)))
 
 
 def launch_count() -> int:

@@ -29,6 +29,13 @@ cudaError_t smem_limit_once(const void* kernel, size_t bytes, std::atomic<int>* 
   return e;
 }
 
+std::atomic<uint64_t> g_wait_ns{0};  // 0: the default bound
+
+uint64_t pipeline_wait_ns() {
+  const uint64_t v = g_wait_ns.load(std::memory_order_relaxed);
+  return v ? v : kWaitLimitNs;
+}
+
 }  // namespace csa2
 
 namespace {
@@ -215,6 +222,7 @@ csa2_status run_index(const csa2_cache& cache, const uint8_t* qpack, const float
   a.err = err;
   a.stages = 16;
   a.tmem_cols = 512u;
+  a.wait_ns = pipeline_wait_ns();
   const int64_t total = a.n_groups * a.tpg;
   const int64_t slots = static_cast<int64_t>(sm_count());  // one persistent CTA per SM
   const int grid = static_cast<int>(total < slots ? total : slots);
@@ -347,6 +355,7 @@ csa2_status run_attn(const csa2_step& s, uint8_t* base, const WsLayout& L, int32
   a.rope_sin = s.rope_sin;
   a.win_ring = s.win_ring;
   a.win_ring_reqs = s.win_ring_reqs;
+  a.wait_ns = pipeline_wait_ns();
   // small batches split each query's key tiles over a cluster of CTAs
   const bool ext = s.sinks != nullptr || s.rope_cos != nullptr || s.win_ring != nullptr;
   a.splits = attn_splits_for(s.n_q, sm_count(), ext);
@@ -558,6 +567,11 @@ csa2_status csa2_check(void* ws, csa2_stream_t stream, int32_t* info) {
 }
 
 int64_t csa2_launch_count(void) { return g_launches.load(); }
+
+csa2_status csa2_debug_set_wait_limit(uint64_t ns) {
+  g_wait_ns.store(ns, std::memory_order_relaxed);
+  return CSA2_OK;
+}
 
 csa2_status csa2_probe_mma(int32_t kind, int32_t n, int32_t iters, int32_t issuers, int32_t n_ctas, int64_t* cycles,
                            csa2_stream_t stream) {

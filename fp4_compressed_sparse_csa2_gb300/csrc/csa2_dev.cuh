@@ -29,7 +29,8 @@ __device__ __forceinline__ void report(int32_t* err, int32_t status, int32_t inf
   if (err != nullptr && atomicCAS(err, 0, status) == 0) atomicExch(err + 1, info);
 }
 
-// Bound for every spin wait: about 2 s of wall time (globaltimer, ns).
+// Default bound of a pipeline wait, and the fixed bound of every wait that drains work
+// already in flight before a CTA exits: about 2 s of wall time (globaltimer, ns).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -129,16 +130,27 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Bounded wait on an mbarrier phase.  A waiting thread is parked by the hardware
 // (suspend-time hint) instead of spinning, so waiting warps leave the issue slots to
 // the warps that work; the wall-clock bound is checked every 16 polls.  Returns false
-// (after at most about kWaitLimitNs) when the phase did not complete or *abort became
+// (after at most about limit_ns) when the phase did not complete or *abort became
 // non-zero.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
+  // a bound below the default (failure-path tests) shortens the suspend hint and is checked
+  // after every poll, so that a wait longer than the bound reliably gives up
+  const bool short_bound = limit_ns < kWaitLimitNs;
+  const uint32_t hint = limit_ns < 20000ull ? static_cast<uint32_t>(limit_ns) : 20000u;
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     if (abort != nullptr && *abort) return false;
-    if ((it & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    if ((short_bound || (it & 15u) == 0) && global_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Wait for work this CTA already has in flight (copies, MMAs) before it exits: the fixed
+// bound, whatever the pipeline limit, and no abort flag.
+__device__ __forceinline__ bool mbar_drain_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait(bar, parity, nullptr, kWaitLimitNs);
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,

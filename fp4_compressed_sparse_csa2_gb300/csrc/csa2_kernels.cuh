@@ -46,6 +46,7 @@ struct IndexArgs {
   int32_t stages;  // smem ring depth
   uint32_t tmem_cols;
   int32_t* err;
+  uint64_t wait_ns;  // bound of each pipeline wait (csa2_debug_set_wait_limit)
 };
 
 struct TopkArgs {
@@ -88,6 +89,7 @@ struct AttnArgs {
   int32_t splits;
   float* opart;  // [n_q * splits][64][512] (splits > 1)
   float* mpart;  // [n_q * splits][2][64]
+  uint64_t wait_ns;  // bound of each pipeline wait (csa2_debug_set_wait_limit)
 };
 
 // Upper bound on the key splits of one query (its five 128-key tiles).
@@ -180,6 +182,9 @@ constexpr int kMaxDevices = 64;
 // kMaxDevices entries of the limit already set.  cudaFuncSetAttribute on every launch
 // leaves the GPU idle between back-to-back launches.
 cudaError_t smem_limit_once(const void* kernel, size_t bytes, std::atomic<int>* cache);
+// The pipeline-wait bound the kernels are launched with (csa2_debug_set_wait_limit; the
+// default about 2 s).
+uint64_t pipeline_wait_ns();
 cudaError_t topk_static_scratch(uint8_t** ptr, size_t* bytes);
 cudaError_t launch_topk_cluster(const TopkArgs& a, int sm_count, cudaStream_t stream);
 size_t attn_smem_bytes();

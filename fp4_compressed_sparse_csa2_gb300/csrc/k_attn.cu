@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
 
     while (cur >= 0) {
       // ---------------------------------------------------------------- S^T of tile cur
-      const bool w_ok = mbar_wait(s_bar, sph, abort);
+      const bool w_ok = mbar_wait(s_bar, sph, abort, a.wait_ns);
       sph ^= 1u;
       if (cbar_or(!(ok && w_ok))) {
         ok = false;
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       for (int c = 0; c < 4; ++c) {
         dequant_chunk(c);
         prefetch_chunk(nx, c);
-        const bool c_ok = mbar_wait(&o_bar[c], oph, abort);
+        const bool c_ok = mbar_wait(&o_bar[c], oph, abort, a.wait_ns);
         if (c_ok) store_chunk(c);
         ok = ok && c_ok;
         chunk_done(c);
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
     if (ok && o_started) {
       bool w_ok = true;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) w_ok &= mbar_wait(&o_bar[c], oph, abort);
+      for (int c = 0; c < 4; ++c) w_ok &= mbar_wait(&o_bar[c], oph, abort, a.wait_ns);
       ok = ok && w_ok;
     }
     if (!ok || *abort) {
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       if (tid == 0) report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
       if (issuer) {  // every MMA this issuer started completes before TMEM is freed
         mma_commit(drain);
-        mbar_wait(drain, 0, nullptr);
+        mbar_drain_wait(drain, 0);
       }
     }
     // ---- per-head sums over the 128 key lanes

@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
       if (!segment(a, g, begin, end, sg)) continue;
       if (lane == 0) {
         const uint32_t slot = m & 1u;
-        ok = mbar_wait(&q_empty[slot], ((m >> 1) & 1u) ^ 1u, abort);
+        ok = mbar_wait(&q_empty[slot], ((m >> 1) & 1u) ^ 1u, abort, a.wait_ns);
         if (ok) {
           mbar_arrive_expect_tx(&q_full[slot], static_cast<uint32_t>(a.grp_bytes));
           bulk_g2s(qslot + slot * kIdxPageBytes, a.qpack + g * a.grp_bytes, static_cast<uint32_t>(a.grp_bytes),
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
         const int32_t left = sg.t1 - t;
         const int32_t cnt = left < static_cast<int32_t>(n_iss - in_st) ? left : static_cast<int32_t>(n_iss - in_st);
         if (in_st == 0) {
-          if (lane == 0) ok = mbar_wait(&empty[k], ph ^ 1u, abort);
+          if (lane == 0) ok = mbar_wait(&empty[k], ph ^ 1u, abort, a.wait_ns);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
@@ -239,7 +239,9 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
       }
     }
     if (lane == 0) {
-      if (ok && n % n_iss != 0) {  // partial last stage
+      // a partial last stage (also one left open when a wait ran out at a group boundary:
+      // its copies are in flight) is closed, so that the drain below waits for it too
+      if (n % n_iss != 0) {
         mbar_arrive(&full[k]);
         ++n_stages;
       }
@@ -249,8 +251,8 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
       }
       // the copies of the last stages land before the CTA exits
       for (uint32_t j = (n_stages > n_st ? n_stages - n_st : 0); j < n_stages; ++j)
-        mbar_wait(&full[j % n_st], (j / n_st) & 1u, nullptr);
-      for (uint32_t j = (m > 2 ? m - 2 : 0); j < m; ++j) mbar_wait(&q_full[j & 1u], (j >> 1) & 1u, nullptr);
+        mbar_drain_wait(&full[j % n_st], (j / n_st) & 1u);
+      for (uint32_t j = (m > 2 ? m - 2 : 0); j < m; ++j) mbar_drain_wait(&q_full[j & 1u], (j >> 1) & 1u);
     }
   } else if (warp >= 1 && warp <= static_cast<int>(n_iss)) {
     if (lane == 0 && static_cast<uint32_t>(warp - 1) < n_iss) {
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
         if (!segment(a, g, begin, end, sg)) continue;
         if (m > 0) mma_commit(&q_empty[(m - 1) & 1u]);  // previous query slot is free once its MMAs finish
         cur = m & 1u;
-        ok = mbar_wait(&q_full[cur], (m >> 1) & 1u, abort);
+        ok = mbar_wait(&q_full[cur], (m >> 1) & 1u, abort, a.wait_ns);
         if (!ok) break;
         tc_fence_after();
         const uint32_t qs = smem_u32(qslot + cur * kIdxPageBytes);
@@ -283,14 +285,14 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
           const uint32_t kst = nn / n_iss;
           const uint32_t s = kst % n_st, ph = (kst / n_st) & 1u;
           const uint32_t b = nn % kAcc, bph = (nn / kAcc) & 1u;
-          ok = mbar_wait(&full[s], ph, abort);
+          ok = mbar_wait(&full[s], ph, abort, a.wait_ns);
           if (!ok) break;
           tc_fence_after();
           const uint32_t st = smem_u32(ring + (s * n_iss + me) * kPg);
           const uint32_t sfa = tmem + (kSplit ? kSfA + 16u * b + 8u * bph : kSfA + 24u * me + 8u * (j % 3u));
           tmem_cp_sf(sfa, sdesc(st + kIdxNibBytes, 128, 128));
           if (!kMx) tmem_cp_sf(sfa + 4, sdesc(st + kIdxNibBytes + 512, 128, 128));
-          ok = mbar_wait(&acc_empty[b], bph ^ 1u, abort);
+          ok = mbar_wait(&acc_empty[b], bph ^ 1u, abort, a.wait_ns);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
         report(a.err, CSA2_ERR_TIMEOUT, kInfoWait);
       }
       mma_commit(&drain[me]);
-      mbar_wait(&drain[me], 0, nullptr);
+      mbar_drain_wait(&drain[me], 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
         }
         // the leader warp waits for the accumulator; the barrier hands its result to the
         // other three warps (which wait there without issuing)
-        const bool got = leader ? mbar_wait(&acc_full[bb], bp, abort) : true;
+        const bool got = leader ? mbar_wait(&acc_full[bb], bp, abort, a.wait_ns) : true;
         if (!named_bar_and(1u + wg, 128u, got)) {
           ok = false;
           break;

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kProbeThreads, 1) probe_mma_kernel(int32_t kin
       tmem_cp_sf(tmem + kSf + 8, sdesc(a0, 128, 128));
       tmem_cp_sf(tmem + kSf + 12, sdesc(a0, 128, 128));
       mma_commit(&bars[4]);  // the copies land before any issuer reads the columns
-      mbar_wait(&bars[4], 0, nullptr);
+      mbar_drain_wait(&bars[4], 0);
     }
   }
   tc_fence_before();
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kProbeThreads, 1) probe_mma_kernel(int32_t kin
       }
     }
     mma_commit(&bars[warp]);
-    mbar_wait(&bars[warp], 0, nullptr);
+    mbar_drain_wait(&bars[warp], 0);
   }
   tc_fence_before();
   __syncthreads();

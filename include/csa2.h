@@ -332,6 +332,15 @@ csa2_status csa2_check(void* ws, csa2_stream_t stream, int32_t* info);
 csa2_status csa2_probe_mma(int32_t kind, int32_t n, int32_t iters, int32_t issuers, int32_t n_ctas, int64_t* cycles,
                            csa2_stream_t stream);
 
+/* Failure-path testing (the pages have no counterpart): sets the bound of every pipeline
+ * wait of the indexer and attention kernels launched afterwards by this process (default
+ * about 2 s; ns = 0 restores it).  A wait that runs out makes the kernel record
+ * CSA2_ERR_TIMEOUT with info 5 in the workspace error word, wait (with the fixed 2 s bound)
+ * for the copies and MMAs it has in flight, free its tensor memory and return; csa2_check
+ * then reports it, and the outputs of that call are undefined.  Not thread-safe with
+ * respect to concurrent launches from other host threads. */
+csa2_status csa2_debug_set_wait_limit(uint64_t ns);
+
 /* Number of kernels this library has launched in this process. */
 int64_t csa2_launch_count(void);
 
