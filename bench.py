@@ -50,6 +50,9 @@ def parse():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before timing (clock sampling)")
     p.add_argument("--no-extra", action="store_true", help="skip the other workloads (tiny, Reuse/Reindex, 1M, prefill)")
+    p.add_argument("--only-prefill", default=None, metavar="N0,N,G",
+                   help="run only a chunked-prefill step of N new tokens on N0 cached entries, index groups of G "
+                        "(--steps / --warmup iterations), print its line and exit (profiling)")
     return p.parse_args()
 
 
@@ -436,6 +439,58 @@ def mma_peaks(dev):
     return out
 
 
+PREFILL_GROUP = 1  # queries per indexer MMA group in the chunked-prefill line
+
+
+def prefill_line(dev, n0, n, group, warmup=2, steps=5, probe=True):
+    """A chunked-prefill step: n new tokens appended causally to n0 cached entries of one
+    request (pack the new entries, causally masked index scores in groups of `group`
+    queries, top-512 per query, attention over the selection and each query's 128-row
+    window), with the indexer's FP4 rate against the probe-measured peak."""
+    import synth
+    from fp4_compressed_sparse_csa2_gb300 import csa2
+    T = n0 + n
+    mp = (T + 127) // 128
+    cache = _device_cache(csa2, dev, 1, n0, mp, 4000)
+    sb = 4000 + 7_000_000
+    new_lat = synth.torch_normal_bf16(sb + 4, (n, D), dev)
+    new_key = synth.torch_normal_bf16(sb + 5, (n, DI), dev)
+    rows = torch.cat([synth.torch_normal_bf16(sb + 6, (127, D), dev), new_lat]).contiguous()
+    step = csa2.make_step(n_q=n, t_max=T, q=synth.torch_normal_bf16(sb + 1, (n, HEADS, D), dev),
+                          req=torch.zeros(n, dtype=torch.int32, device=dev),
+                          n_visible=torch.arange(n0 + 1, T + 1, dtype=torch.int32, device=dev), window=rows,
+                          win_start=torch.arange(n, dtype=torch.int64, device=dev),
+                          win_len=torch.full((n,), WIN, dtype=torch.int32, device=dev), cache=cache,
+                          topk_idx=torch.empty((n, TOPK), dtype=torch.int32, device=dev),
+                          out=torch.empty((n, HEADS, D), dtype=torch.bfloat16, device=dev),
+                          lse=torch.empty((n, HEADS), dtype=torch.float32, device=dev),
+                          q_idx=synth.torch_normal_bf16(sb + 2, (n, HEADS_I, DI), dev),
+                          w=synth.torch_normal_f32(sb + 3, (n, HEADS_I), dev), heads_I=HEADS_I, group=group,
+                          n_new=n, new_latent=new_lat, new_idx_key=new_key,
+                          new_req=torch.zeros(n, dtype=torch.int32, device=dev),
+                          new_pos=torch.arange(n0, T, dtype=torch.int64, device=dev))
+    ws = csa2.alloc_workspace(n, HEADS_I, T, True, dev)
+    ms, kernels = _timed(csa2, lambda: csa2.sparse_attn_full(step, ws), warmup, steps)
+    st, _ = csa2.check(ws)
+    pairs = n * n0 + n * (n + 1) // 2                 # visible (query, entry) pairs
+    flops = pairs * HEADS_I * DI * 2
+    del step, ws, cache
+    torch.cuda.empty_cache()
+    line = {"workload": f"chunked prefill: {n} new tokens on {n0} cached entries, index groups of {group}",
+            "metric": "chunk-steps/s", "value": round(1000.0 / ms, 3), "ms_per_step": round(ms, 3),
+            "kernels_us": kernels, "index_flops": flops, "device_status": st}
+    idx_tf = flops / (kernels.get("index", float("nan")) * 1e-6) / 1e12
+    line["index_tflops"] = round(idx_tf, 1)
+    if probe:
+        pk = mma_peaks(dev)
+        line.update({"index_fp4_frac": round(idx_tf / pk["nvf4_peak_tflops"], 4),
+                     "fp4_peak_tflops": round(pk["nvf4_peak_tflops"], 1),
+                     "fp4_peak_source": "measured: csa2_probe_mma, back-to-back block-scaled NVFP4 tcgen05.mma "
+                                        "(M=128, best of N and issuer counts) on every SM, CUDA events",
+                     "mma_probe": pk})
+    return line
+
+
 def measure_extra(dev, hbm_peak, bf16_tflops):
     """The other workloads of the layer, each in its own line: the tiny decode, Reuse and
     Reindex at 128 x 262,144, the headline decode with sinks and fused partial RoPE, with the
@@ -538,48 +593,7 @@ def measure_extra(dev, hbm_peak, bf16_tflops):
     attempt(lambda: dict(_decode_line(csa2, dev, "ratio-2 layer Full decode, B=8, 524288 pooled entries, 1% x8", 8,
                                       1 << 19, 3100, 0.01), note="encoder-style layer of the same step"))
 
-    def prefill():
-        n0, n = 262144, 4096
-        T = n0 + n
-        mp = T // 128
-        cache = _device_cache(csa2, dev, 1, n0, mp, 4000)
-        sb = 4000 + 7_000_000
-        new_lat = synth.torch_normal_bf16(sb + 4, (n, D), dev)
-        new_key = synth.torch_normal_bf16(sb + 5, (n, DI), dev)
-        rows = torch.cat([synth.torch_normal_bf16(sb + 6, (127, D), dev), new_lat]).contiguous()
-        step = csa2.make_step(n_q=n, t_max=T, q=synth.torch_normal_bf16(sb + 1, (n, HEADS, D), dev),
-                              req=torch.zeros(n, dtype=torch.int32, device=dev),
-                              n_visible=torch.arange(n0 + 1, T + 1, dtype=torch.int32, device=dev), window=rows,
-                              win_start=torch.arange(n, dtype=torch.int64, device=dev),
-                              win_len=torch.full((n,), WIN, dtype=torch.int32, device=dev), cache=cache,
-                              topk_idx=torch.empty((n, TOPK), dtype=torch.int32, device=dev),
-                              out=torch.empty((n, HEADS, D), dtype=torch.bfloat16, device=dev),
-                              lse=torch.empty((n, HEADS), dtype=torch.float32, device=dev),
-                              q_idx=synth.torch_normal_bf16(sb + 2, (n, HEADS_I, DI), dev),
-                              w=synth.torch_normal_f32(sb + 3, (n, HEADS_I), dev), heads_I=HEADS_I, group=2,
-                              n_new=n, new_latent=new_lat, new_idx_key=new_key,
-                              new_req=torch.zeros(n, dtype=torch.int32, device=dev),
-                              new_pos=torch.arange(n0, T, dtype=torch.int64, device=dev))
-        ws = csa2.alloc_workspace(n, HEADS_I, T, True, dev)
-        ms, kernels = _timed(csa2, lambda: csa2.sparse_attn_full(step, ws), 2, 5)
-        st, _ = csa2.check(ws)
-        pairs = n * n0 + n * (n + 1) // 2                 # visible (query, entry) pairs
-        flops = pairs * HEADS_I * DI * 2
-        del step, ws, cache
-        torch.cuda.empty_cache()
-        probe = mma_peaks(dev)
-        fp4_peak = probe["nvf4_peak_tflops"]
-        idx_tf = flops / (kernels.get("index", float("nan")) * 1e-6) / 1e12
-        return {"workload": "chunked prefill: 4096 new tokens on 262144 cached entries, index groups of 2",
-                "metric": "chunk-steps/s", "value": round(1000.0 / ms, 3), "ms_per_step": round(ms, 3),
-                "kernels_us": kernels, "index_tflops": round(idx_tf, 1),
-                "index_fp4_frac": round(idx_tf / fp4_peak, 4),
-                "fp4_peak_tflops": round(fp4_peak, 1),
-                "fp4_peak_source": "measured: csa2_probe_mma, back-to-back block-scaled NVFP4 tcgen05.mma "
-                                   "(M=128, best of N and issuer counts) on every SM, CUDA events",
-                "mma_probe": probe, "index_flops": flops, "device_status": st}
-
-    attempt(prefill)
+    attempt(lambda: prefill_line(dev, 262144, 4096, PREFILL_GROUP))
     return lines
 
 def host_cores():
@@ -784,6 +798,12 @@ def run_reference(args, ws, rank, local):
 
 def main():
     args = parse()
+    if args.only_prefill:
+        n0, n, g = (int(x) for x in args.only_prefill.split(","))
+        dev = torch.device("cuda", 0)
+        print(json.dumps(prefill_line(dev, n0, n, g, warmup=max(args.warmup, 1), steps=max(args.steps, 1),
+                                      probe=False)), flush=True)
+        return
     ws, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, ws, rank, local)

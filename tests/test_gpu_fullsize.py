@@ -228,9 +228,11 @@ def test_reuse_and_reindex_128x262144(orc, csa2):
                       windows=[(0, 4096), (123 * PAGE, 123 * PAGE + 4096), (T - 4096, T)])
 
 
-def test_chunked_prefill_4096_on_262144(orc, csa2):
+@pytest.mark.parametrize("group", [1, 2])
+def test_chunked_prefill_4096_on_262144(orc, csa2, group):
     # one request: 262144 cached entries, 4096 new tokens packed by the step and queried
-    # causally (query i sees entries 0 .. n0 + i); indexer groups of two queries
+    # causally (query i sees entries 0 .. n0 + i); indexer groups of one query (the
+    # benchmark's prefill line) and of two
     n0, n_new = 262144, 4096
     T = n0 + n_new
     mp = T // PAGE
@@ -247,7 +249,7 @@ def test_chunked_prefill_4096_on_262144(orc, csa2):
     new = dict(n=n_new, lat=new_lat, key=new_key, req=torch.zeros(n_new, dtype=torch.int32, device="cuda"),
                pos=torch.arange(n0, T, dtype=torch.int64, device="cuda"))
     nvis = torch.arange(n0 + 1, T + 1, dtype=torch.int32, device="cuda")
-    res = _full_step(csa2, dc, 1, T, 550600, group=2, n_q=n_new, req=torch.zeros(n_new, dtype=torch.int32,
+    res = _full_step(csa2, dc, 1, T, 550600, group=group, n_q=n_new, req=torch.zeros(n_new, dtype=torch.int32,
                      device="cuda"), nvis=nvis, win=win, new=new)
     idx = res["topk_idx"].cpu().numpy()
     q, q_idx, w = host_bits(res["q"]), host_bits(res["q_idx"]), res["w"].cpu().numpy()
