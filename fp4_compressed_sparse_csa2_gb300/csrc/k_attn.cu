@@ -18,7 +18,8 @@
 //             tile t+1 is dequantised into each freed chunk (its records were loaded into
 //             registers one tile ahead) while the later O chunks and the S MMAs of the
 //             chunks already built run on the tensor pipe;
-//   S^T      tcgen05.mma kind::f16, M = 128 keys, N = 64 heads, K = 512 (TMEM cols 256..319);
+//   S^T      tcgen05.mma kind::f16, M = 128 keys, N = 64 heads, K = 512, as two partial sums
+//             over alternate channel chunks (TMEM cols 256..383);
 //   softmax  thread = key, 16 heads per thread: a block-wide vote finds whether any score
 //             exceeds its head's reference maximum by 2^8; only then are the reference
 //             maxima raised (warp max reductions) and O^T and the running sums rescaled;
@@ -43,7 +44,7 @@ constexpr int kHeads = 64;
 constexpr uint32_t kKtBytes = 128 * 512 * 2;  // f16 key/value tile
 constexpr uint32_t kQsBytes = 64 * 512 * 2;   // f16 queries, all heads
 constexpr uint32_t kPsBytes = 128 * 64 * 2;   // f16 P^T
-constexpr uint32_t kSCol = 256;               // TMEM: O^T chunk c at columns 64c.., S^T partial c at 256 + 64c
+constexpr uint32_t kSCol = 256;               // TMEM: O^T chunk c at columns 64c.., S^T partial i at 256 + 64i
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 // shared memory map (bytes)
 constexpr uint32_t kOffQs = kKtBytes;
@@ -131,9 +132,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // MMA issuers: lane 0 of warps 0..3; issuer c owns 128-channel chunk c (its S partial sum
-  // and its O chunk), so no two issuers accumulate into one TMEM region
-  const bool issuer = warp < 4 && lane == 0;
+  // Two MMA-issuing threads, lane 0 of warps 0 and 1 (one thread issues a dependent MMA
+  // about every 66 cycles, two keep the tensor pipe busy): issuer i owns the 128-channel
+  // chunks c with c % 2 == i (their S^T partial i and their O^T chunks).  Building warps
+  // hand each built chunk over with a non-blocking barrier arrival and only the chunk's
+  // issuer warp waits there, so an MMA issue that stalls on a full tensor-core queue holds
+  // up that warp alone.
+  const bool issuer = warp < 2 && lane == 0;
   const int qd = warp & 3;   // TMEM lane quarter of this warp
   const int hg = warp >> 2;  // head group: heads [16 hg, 16 hg + 16) in the softmax, O chunk hg
   const int S = a.splits;    // CTAs per query (one cluster)
@@ -150,9 +155,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   const bool win_tile = has_win && wl > 0;  // an empty window is no tile
 
   if (tid == 0) {
-    mbar_init(s_bar, 4);  // one commit per issuer
+    mbar_init(s_bar, 2);  // one commit per issuer and tile, after its last S^T chunk
     for (int i = 0; i < 4; ++i) mbar_init(&o_bar[i], 1);
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);  // one commit per issuer
     *abort = 0;
     fence_mbar_init();
   }
@@ -288,52 +293,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   uint32_t oph = 0;  // parity of the next O completion
   const uint32_t idesc_s = idesc_f16(128, kHeads, 0, 0);
   const uint32_t idesc_o = idesc_f16(128, kHeads, 1, 1);
-  // issuer c: S partial c over the channels of chunk c (called after the block barrier that
-  // follows the chunk's build)
+  // S^T partial (c % 2) += K_c Q_c^T over the channels of chunk c (its issuer, once the
+  // chunk is built); both partials are complete after chunks 2 and 3
   auto issue_s = [&](int c) {
-    if (issuer && warp == c) {
+    if (issuer && warp == (c & 1)) {
       const uint64_t dK0 = sdesc(smem_u32(Kt), 128, 8192), dQ0 = sdesc(smem_u32(Qs), 128, 8192);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        mma_f16(tmem + kSCol + 64u * c, dK0 + static_cast<uint64_t>(16 * (8 * c + k)),
-                dQ0 + static_cast<uint64_t>(16 * (8 * c + k)), idesc_s, k > 0 ? 1u : 0u);
-      mma_commit(s_bar);
+        mma_f16(tmem + kSCol + 64u * static_cast<uint32_t>(c & 1), dK0 + static_cast<uint64_t>(16 * (8 * c + k)),
+                dQ0 + static_cast<uint64_t>(16 * (8 * c + k)), idesc_s, (c > 1 || k > 0) ? 1u : 0u);
+      if (c > 1) mma_commit(s_bar);
     }
   };
-  // issuer c: O chunk c (called after the block barrier that follows the P stores)
+  // O^T chunks (issuer i: i, then i + 2; after the block barrier that follows the P
+  // stores); o_bar[c] completes when chunk c has been computed
   auto issue_o = [&]() {
     if (issuer) {
-      const uint32_t c = static_cast<uint32_t>(warp);
       const uint64_t dV0 = sdesc(smem_u32(Kt), 8192, 128), dP0 = sdesc(smem_u32(Ps), 1024, 128);
 #pragma unroll
-      for (uint32_t kk = 0; kk < 8; ++kk)
-        mma_f16(tmem + 64u * c, dV0 + static_cast<uint64_t>(128u * c + 1024u * kk),
-                dP0 + static_cast<uint64_t>(128u * kk), idesc_o, (o_started || kk > 0) ? 1u : 0u);
-      mma_commit(&o_bar[c]);
+      for (uint32_t j = 0; j < 2; ++j) {
+        const uint32_t c = static_cast<uint32_t>(warp) + 2u * j;
+#pragma unroll
+        for (uint32_t kk = 0; kk < 8; ++kk)
+          mma_f16(tmem + 64u * c, dV0 + static_cast<uint64_t>(128u * c + 1024u * kk),
+                  dP0 + static_cast<uint64_t>(128u * kk), idesc_o, (o_started || kk > 0) ? 1u : 0u);
+        mma_commit(&o_bar[c]);
+      }
     }
   };
   {
     // ================================================================ the tiles
     // register prefetch of a selected tile: thread = (key 8 warp + lane % 8, 32-channel
-    // piece lane / 8 of each 128-channel chunk); per chunk 16 bytes of nibbles, 2 scale bytes
+    // piece lane / 8 of each 128-channel chunk); per chunk 16 bytes of nibbles.  The
+    // record's 32 scale bytes are loaded once per tile, 16 bytes by each of the key's
+    // lanes with piece 0 and 1 (chunks 0-1 and 2-3), and handed to the other lanes by
+    // shuffles: the narrow per-chunk scale loads doubled the load instructions that the
+    // memory pipeline accepts only slowly for scattered records.
     const uint32_t bkey = static_cast<uint32_t>(8 * warp + (lane & 7));
     const uint32_t bj = static_cast<uint32_t>(lane >> 3);
     uint4 pn[4];
-    uint32_t ps[4];
-    auto prefetch_chunk = [&](int ts, int c) {  // chunk c of selected tile ts (ts < 0 or 4: nothing)
+    uint4 sq = make_uint4(0u, 0u, 0u, 0u);
+    // chunk c of selected tile ts (ts < 0 or 4: nothing); c == 3 also loads the scales (the
+    // current tile's are no longer needed once its last chunk is dequantised)
+    auto prefetch_chunk = [&](int ts, int c) {
       const int32_t rid = (ts < 0 || ts == 4) ? -1 : recid[ts * 128 + static_cast<int>(bkey)];
       if (rid >= 0) {
         const uint8_t* rec = a.cache.kv + static_cast<int64_t>(rid) * kKvBytes;
         pn[c] = __ldg(reinterpret_cast<const uint4*>(rec + 64 * c + 16 * bj));
-        ps[c] = __ldg(reinterpret_cast<const unsigned short*>(rec + 256 + 8 * c + 2 * bj));
+        if (c == 3 && bj < 2u) sq = __ldg(reinterpret_cast<const uint4*>(rec + 256 + 16 * bj));
       } else {  // no entry: zeros (masked below)
         pn[c] = make_uint4(0u, 0u, 0u, 0u);
-        ps[c] = 0u;
+        if (c == 3) sq = make_uint4(0u, 0u, 0u, 0u);
       }
     };
     uint32_t dq[16];
     auto dequant_chunk = [&](int c) {  // registers -> 32 f16 values of this thread's piece
-      const uint32_t sc2 = e4m3x2_f16x2_bits(ps[c]);
+      // scale bytes 8c + 2bj, 8c + 2bj + 1 of the record: word 2 (c % 2) + bj / 2, half
+      // bj % 2 of the 16 bytes held by the key's lane with piece c / 2
+      const uint32_t src = (static_cast<uint32_t>(lane) & 7u) + 8u * static_cast<uint32_t>(c >> 1);
+      const uint32_t w0 = __shfl_sync(0xffffffffu, (c & 1) ? sq.z : sq.x, static_cast<int>(src));
+      const uint32_t w1 = __shfl_sync(0xffffffffu, (c & 1) ? sq.w : sq.y, static_cast<int>(src));
+      const uint32_t wsel = (bj >> 1) ? w1 : w0;
+      const uint32_t sc2 = e4m3x2_f16x2_bits((bj & 1u) ? (wsel >> 16) : (wsel & 0xFFFFu));
       const uint32_t s0 = prmt(sc2, sc2, 0x1010u), s1 = prmt(sc2, sc2, 0x3232u);
       const uint32_t wds[4] = {pn[c].x, pn[c].y, pn[c].z, pn[c].w};
 #pragma unroll
@@ -350,12 +371,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         *reinterpret_cast<uint4*>(Kt + tile_off(bkey, 128u * c + 32u * bj + 8u * m)) =
             make_uint4(dq[4 * m], dq[4 * m + 1], dq[4 * m + 2], dq[4 * m + 3]);
     };
-    auto chunk_done = [&](int c) {  // chunk c is in place (and every S load is done): its S MMAs
+    // chunk c is in place (and every S load is done): the chunk's issuer warp waits for
+    // every warp's part and issues its S MMAs; the other warps arrive and go on
+    auto chunk_done = [&](int c) {
       fence_proxy_async_smem();
       tc_fence_before();
-      cbar_sync();
-      tc_fence_after();
-      issue_s(c);
+      if (warp == (c & 1)) {
+        named_bar_sync(2u + static_cast<uint32_t>(c), 512u);
+        tc_fence_after();
+        issue_s(c);
+      } else {
+        named_bar_arrive(2u + static_cast<uint32_t>(c), 512u);
+      }
     };
 
     int cur = first;
@@ -367,7 +394,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         cp_async_wait_all();
         cbar_sync();  // every thread's window pieces have landed
       }
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (!ring) {
 #pragma unroll
@@ -410,21 +437,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       // ---------------------------------------------------------------- softmax
       const bool kv_ok = cur == 4 ? static_cast<int32_t>(key) < wl : recid[cur * 128 + key] >= 0;
       float x[16];
-      {  // the four partial sums, two at a time
+      {  // the two partial sums
         uint32_t r[2][16];
+        tmem_ld16(tmem + lane_base + kSCol + static_cast<uint32_t>(h0), r[0]);
+        tmem_ld16(tmem + lane_base + kSCol + 64u + static_cast<uint32_t>(h0), r[1]);
+        tmem_ld_wait();
 #pragma unroll
-        for (int p = 0; p < 4; p += 2) {
-          tmem_ld16(tmem + lane_base + kSCol + 64u * p + static_cast<uint32_t>(h0), r[0]);
-          tmem_ld16(tmem + lane_base + kSCol + 64u * (p + 1) + static_cast<uint32_t>(h0), r[1]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float v = __uint_as_float(r[0][i]) + __uint_as_float(r[1][i]);
-            x[i] = p == 0 ? v : x[i] + v;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = kv_ok ? x[i] * a.scale_log2 : -INFINITY;
+        for (int i = 0; i < 16; ++i)
+          x[i] = kv_ok ? (__uint_as_float(r[0][i]) + __uint_as_float(r[1][i])) * a.scale_log2 : -INFINITY;
       }
       // the reference maxima live in shared memory (ref_s), read as broadcasts
       bool need = false, rescale = false;
