@@ -574,29 +574,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   // ---------------------------------------------------------------- epilogue
   const uint32_t d = static_cast<uint32_t>(128 * hg + 32 * qd + lane);  // output channel (O^T lane)
   const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-  if (S == 1) {
+  // One CTA per query, or the second of a pair: it writes the output itself, the second
+  // of a pair adding the first one's partial (written to the workspace before the pair's
+  // cluster barrier) instead of both writing partials and splitting the heads.
+  if (S == 1 || (S == 2 && sp == 1)) {
+    const float* part0 = a.opart + static_cast<int64_t>(qi) * 2 * kHeads * CSA2_D;  // rank 0's [64][512]
+    if (S == 2) attn_cluster_sync();  // rank 0's partial and (max, sum) are written and visible
     __syncthreads();
     if (tid < kHeads) {
-      const float l = ml[kHeads + tid], m = ml[tid];
-      float lse2 = -INFINITY, inv = 0.0f;  // log2 sum-exp; O = O^T * inv
-      if (!kExt || a.sinks == nullptr) {
-        if (l > 0.0f) {
-          lse2 = m + log2f(l);
-          inv = 1.0f / l;
-        }
-      } else {
-        // the sink joins the denominator: O = O^T / (l + 2^(sink - ref)), taken relative to
-        // the larger of the two maxima so that nothing overflows
-        const float sk = __ldg(a.sinks + tid) * 1.4426950408889634f;
-        if (l > 0.0f || sk != -INFINITY) {
-          const float m2 = l > 0.0f ? fmaxf(m, sk) : sk;
-          const float lt = (l > 0.0f ? l * exp2f(m - m2) : 0.0f) + exp2f(sk - m2);
-          lse2 = m2 + log2f(lt);
-          inv = l > 0.0f ? exp2f(m - m2) / lt : 0.0f;
-        }
+      // O = (2^(m1 - M) O1^T + 2^(m0 - M) O0) / L with L = sum over the parts (and the sink)
+      // of l 2^(m - M), relative to the largest maximum M of the non-empty parts
+      const float l1 = ml[kHeads + tid], m1 = ml[tid];
+      const float l0 = S == 2 ? __ldcg(a.mpart + qi * 2 * 2 * kHeads + kHeads + tid) : 0.0f;
+      const float m0 = S == 2 ? __ldcg(a.mpart + qi * 2 * 2 * kHeads + tid) : -INFINITY;
+      const float sk = (kExt && a.sinks != nullptr) ? __ldg(a.sinks + tid) * 1.4426950408889634f : -INFINITY;
+      float M = sk;
+      if (l1 > 0.0f) M = fmaxf(M, m1);
+      if (l0 > 0.0f) M = fmaxf(M, m0);
+      float lse2 = -INFINITY, w1 = 0.0f, w0 = 0.0f;  // log2 sum-exp and the parts' weights
+      if (M != -INFINITY) {
+        const float e1 = l1 > 0.0f ? exp2f(m1 - M) : 0.0f, e0 = l0 > 0.0f ? exp2f(m0 - M) : 0.0f;
+        const float L = l1 * e1 + l0 * e0 + (sk != -INFINITY ? exp2f(sk - M) : 0.0f);
+        lse2 = M + log2f(L);
+        w1 = e1 / L;
+        w0 = e0 / L;
       }
       if (a.lse) a.lse[qi * kHeads + tid] = lse2 * 0.6931471805599453f;
-      alpha[tid] = inv;
+      alpha[tid] = w1;
+      ref_s[tid] = w0;  // the reference maxima are in ml now
     }
     __syncthreads();
     // O^T (TMEM lane = channel, column = head) -> bf16 straight to the output: for each
@@ -612,9 +617,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
           tmem_ld_wait();
         }
 #pragma unroll
+        float p0[32];  // rank 0's partial for these heads (S == 2), all loads issued first
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p0[i] = S == 2 ? __ldcg(part0 + (32 * half + i) * CSA2_D + d) : 0.0f;
+#pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int h = 32 * half + i;
-          const float o = have_o ? __uint_as_float(r[i]) * alpha[h] : 0.0f;
+          const float o = (have_o ? __uint_as_float(r[i]) * alpha[h] : 0.0f) + (S == 2 ? p0[i] * ref_s[h] : 0.0f);
           if (rope && d >= 448u)
             otail[h * 64 + (d - 448u)] = o;
           else
@@ -637,8 +646,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
   } else {
     // ---- merge of the cluster's partials through L2: every CTA writes its raw O^T
     // (relative to its own reference maxima) and its (max, sum) per head to the workspace;
-    // after one cluster barrier rank r combines heads [64 r / S, 64 (r + 1) / S).  Every CTA
-    // reaches the barrier, also after a failed wait (its partial then counts as empty).
+    // after one cluster barrier rank r combines heads [64 r / S, 64 (r + 1) / S) (S > 2; with
+    // S == 2 rank 0 only writes, see above).  Every CTA reaches the barrier, also after a
+    // failed wait (its partial then counts as empty).
     float* opart = a.opart + static_cast<int64_t>(blockIdx.x) * kHeads * CSA2_D;  // [64][512]
     float* mpart = a.mpart + static_cast<int64_t>(blockIdx.x) * 2 * kHeads;       // [2][64]
     {
@@ -658,88 +668,90 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       mpart[kHeads + tid] = ml[kHeads + tid];
     }
     attn_cluster_sync();  // every partial of the cluster is written and visible
-    const int hlo = kHeads * sp / S, hhi = kHeads * (sp + 1) / S;
-    const float* opart0 = a.opart + static_cast<int64_t>(qi) * S * kHeads * CSA2_D;
-    const float* mpart0 = a.mpart + static_cast<int64_t>(qi) * S * 2 * kHeads;
-    float* fs = reinterpret_cast<float*>(Ps);  // [S][64] weight of each rank's partial
-    float* otail = fs + kAttnMaxSplits * kHeads;  // [owned heads][64] fp32 rotated channels (RoPE)
-    if (tid >= hlo && tid < hhi) {
-      float mr[kAttnMaxSplits], lr[kAttnMaxSplits];
-      float M = -INFINITY;
+    if (S > 2) {  // rank 0 of a pair is done: rank 1 adds its partial
+      const int hlo = kHeads * sp / S, hhi = kHeads * (sp + 1) / S;
+      const float* opart0 = a.opart + static_cast<int64_t>(qi) * S * kHeads * CSA2_D;
+      const float* mpart0 = a.mpart + static_cast<int64_t>(qi) * S * 2 * kHeads;
+      float* fs = reinterpret_cast<float*>(Ps);  // [S][64] weight of each rank's partial
+      float* otail = fs + kAttnMaxSplits * kHeads;  // [owned heads][64] fp32 rotated channels (RoPE)
+      if (tid >= hlo && tid < hhi) {
+        float mr[kAttnMaxSplits], lr[kAttnMaxSplits];
+        float M = -INFINITY;
 #pragma unroll
-      for (int r = 0; r < kAttnMaxSplits; ++r) {
-        mr[r] = r < S ? __ldcg(mpart0 + r * 2 * kHeads + tid) : -INFINITY;
-        lr[r] = r < S ? __ldcg(mpart0 + r * 2 * kHeads + kHeads + tid) : 0.0f;
-        if (lr[r] > 0.0f) M = fmaxf(M, mr[r]);
+        for (int r = 0; r < kAttnMaxSplits; ++r) {
+          mr[r] = r < S ? __ldcg(mpart0 + r * 2 * kHeads + tid) : -INFINITY;
+          lr[r] = r < S ? __ldcg(mpart0 + r * 2 * kHeads + kHeads + tid) : 0.0f;
+          if (lr[r] > 0.0f) M = fmaxf(M, mr[r]);
+        }
+        float sk = -INFINITY;
+        if (kExt && a.sinks != nullptr) sk = __ldg(a.sinks + tid) * 1.4426950408889634f;
+        const float M2 = fmaxf(M, sk);
+        float L = sk != -INFINITY ? exp2f(sk - M2) : 0.0f;
+#pragma unroll
+        for (int r = 0; r < kAttnMaxSplits; ++r)
+          if (lr[r] > 0.0f) L += lr[r] * exp2f(mr[r] - M2);
+#pragma unroll
+        for (int r = 0; r < kAttnMaxSplits; ++r)
+          if (r < S) fs[r * kHeads + tid] = (lr[r] > 0.0f && L > 0.0f) ? exp2f(mr[r] - M2) / L : 0.0f;
+        if (a.lse) a.lse[qi * kHeads + tid] = L > 0.0f ? (M2 + log2f(L)) * 0.6931471805599453f : -INFINITY;
       }
-      float sk = -INFINITY;
-      if (kExt && a.sinks != nullptr) sk = __ldg(a.sinks + tid) * 1.4426950408889634f;
-      const float M2 = fmaxf(M, sk);
-      float L = sk != -INFINITY ? exp2f(sk - M2) : 0.0f;
-#pragma unroll
-      for (int r = 0; r < kAttnMaxSplits; ++r)
-        if (lr[r] > 0.0f) L += lr[r] * exp2f(mr[r] - M2);
-#pragma unroll
-      for (int r = 0; r < kAttnMaxSplits; ++r)
-        if (r < S) fs[r * kHeads + tid] = (lr[r] > 0.0f && L > 0.0f) ? exp2f(mr[r] - M2) / L : 0.0f;
-      if (a.lse) a.lse[qi * kHeads + tid] = L > 0.0f ? (M2 + log2f(L)) * 0.6931471805599453f : -INFINITY;
-    }
-    __syncthreads();
-    // items of 4 channels of one owned head: the S partials with 16-byte loads, weighted,
-    // -> bf16 (with RoPE the last 64 channels go through otail and are rotated below).  A
-    // thread's items are at most 8 (32 heads x 128 groups / 512 threads); all of their loads
-    // are issued before the first is used.
-    const int items = (hhi - hlo) * (CSA2_D / 4);
-    float4 accs[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) accs[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0; r < S; ++r) {
-      float4 v[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int it = tid + kComputeThreads * k;
-        const int h = hlo + it / (CSA2_D / 4), g = it % (CSA2_D / 4);
-        v[k] = it < items ? __ldcg(reinterpret_cast<const float4*>(opart0 + (static_cast<int64_t>(r) * kHeads + h) * CSA2_D) + g)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int it = tid + kComputeThreads * k;
-        const int h = hlo + (it < items ? it / (CSA2_D / 4) : 0);
-        const float f = fs[r * kHeads + h];
-        accs[k].x += f * v[k].x;
-        accs[k].y += f * v[k].y;
-        accs[k].z += f * v[k].z;
-        accs[k].w += f * v[k].w;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int it = tid + kComputeThreads * k;
-      if (it >= items) break;
-      const int h = hlo + it / (CSA2_D / 4), g = it % (CSA2_D / 4);
-      const float4 acc = accs[k];
-      if (rope && g >= 112) {
-        float* t = otail + (h - hlo) * 64 + (4 * g - 448);
-        t[0] = acc.x;
-        t[1] = acc.y;
-        t[2] = acc.z;
-        t[3] = acc.w;
-      } else {
-        const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(a.out + (qi * kHeads + h) * CSA2_D + 4 * g) =
-            make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
-      }
-    }
-    if (rope) {
       __syncthreads();
-      for (int p = tid; p < (hhi - hlo) * 32; p += kAttnThreads) {
-        const int hh = p >> 5, i = p & 31;
-        const float c = __ldg(a.rope_cos + qi * 32 + i), sn = __ldg(a.rope_sin + qi * 32 + i);
-        const float x = otail[hh * 64 + i], y = otail[hh * 64 + 32 + i];
-        __nv_bfloat16* dst = a.out + (qi * kHeads + hlo + hh) * CSA2_D;
-        dst[448 + i] = __float2bfloat16_rn(x * c + y * sn);
-        dst[480 + i] = __float2bfloat16_rn(y * c - x * sn);
+      // items of 4 channels of one owned head: the S partials with 16-byte loads, weighted,
+      // -> bf16 (with RoPE the last 64 channels go through otail and are rotated below).  A
+      // thread's items are at most 8 (32 heads x 128 groups / 512 threads); all of their loads
+      // are issued before the first is used.
+      const int items = (hhi - hlo) * (CSA2_D / 4);
+      float4 accs[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) accs[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < S; ++r) {
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int it = tid + kComputeThreads * k;
+          const int h = hlo + it / (CSA2_D / 4), g = it % (CSA2_D / 4);
+          v[k] = it < items ? __ldcg(reinterpret_cast<const float4*>(opart0 + (static_cast<int64_t>(r) * kHeads + h) * CSA2_D) + g)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int it = tid + kComputeThreads * k;
+          const int h = hlo + (it < items ? it / (CSA2_D / 4) : 0);
+          const float f = fs[r * kHeads + h];
+          accs[k].x += f * v[k].x;
+          accs[k].y += f * v[k].y;
+          accs[k].z += f * v[k].z;
+          accs[k].w += f * v[k].w;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int it = tid + kComputeThreads * k;
+        if (it >= items) break;
+        const int h = hlo + it / (CSA2_D / 4), g = it % (CSA2_D / 4);
+        const float4 acc = accs[k];
+        if (rope && g >= 112) {
+          float* t = otail + (h - hlo) * 64 + (4 * g - 448);
+          t[0] = acc.x;
+          t[1] = acc.y;
+          t[2] = acc.z;
+          t[3] = acc.w;
+        } else {
+          const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
+          *reinterpret_cast<uint2*>(a.out + (qi * kHeads + h) * CSA2_D + 4 * g) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+        }
+      }
+      if (rope) {
+        __syncthreads();
+        for (int p = tid; p < (hhi - hlo) * 32; p += kAttnThreads) {
+          const int hh = p >> 5, i = p & 31;
+          const float c = __ldg(a.rope_cos + qi * 32 + i), sn = __ldg(a.rope_sin + qi * 32 + i);
+          const float x = otail[hh * 64 + i], y = otail[hh * 64 + 32 + i];
+          __nv_bfloat16* dst = a.out + (qi * kHeads + hlo + hh) * CSA2_D;
+          dst[448 + i] = __float2bfloat16_rn(x * c + y * sn);
+          dst[480 + i] = __float2bfloat16_rn(y * c - x * sn);
+        }
       }
     }
   }
