@@ -746,7 +746,7 @@ def run_ours(args, ws, rank, local):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp4e2m1 x fp4e2m1 (indexer), bf16 (attention), fp32 acc",
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp4e2m1 x fp4e2m1 (indexer), f16 (attention), fp32 acc",
             "data": "synthetic (seeded N(0,1) latents, keys, queries; fp32 N(0,1) head weights)",
             "config": {"workload": workload_name(wl.B, wl.T), "global_batch": wl.B * ws, "seq_len": wl.T,
                        "parallelism": f"replicas x{ws} (requests sharded, no collective)",
