@@ -104,12 +104,13 @@ def test_attn_shared_window_rows_prefill_style(orc, csa2):
     _reuse(orc, csa2, n, idx, [0] * n_q, [128, 128, 128], seed=53, win_rows=130)
 
 
-@pytest.mark.parametrize("n_q", [3, 80])
+@pytest.mark.parametrize("n_q", [3, 45, 64, 80])
 def test_attn_sinks_and_partial_rope(orc, csa2, n_q):
     """Per-head sinks join the softmax; the query's trailing 64 channels are rotated at
     its position and the output rotated back ("From MLA to DSA to HCA/CSA", "The sliding
-    window" and "What replaced MLA").  3 queries take the cluster merge (5 CTAs each), 80
-    one CTA each."""
+    window" and "What replaced MLA").  On 152 SMs: 3 queries take 5 CTAs each and 45 take
+    3 (every CTA combines a slice of the heads), 64 take a pair (the second CTA adds the
+    first one's partial, sinks and rotation in its epilogue), 80 one CTA each."""
     n = [1800]
     idx = np.stack([synth.distinct_indices(20 + i, 1800, 512) for i in range(n_q)])
     idx[-1, 100:] = -1                   # a short selection
@@ -155,8 +156,9 @@ def test_attn_bounded_replay_window(orc, csa2):
 @pytest.mark.parametrize("n_q", [3, 34, 45, 60, 80])
 def test_attn_key_tile_splits(orc, csa2, n_q):
     """Batches smaller than the SM count split each query's key tiles over a cluster of CTAs
-    that merge their partial outputs by their sums of exponentials through distributed
-    shared memory; on 152 SMs these batch sizes take 5, 4, 3, 2 and 1 CTAs per query.  Rows
+    that merge their partial outputs by their maxima and sums of exponentials (partials in
+    the workspace, one cluster barrier); on 152 SMs these batch sizes take 5, 4, 3, 2 and 1
+    CTAs per query.  Rows
     mix full selections, short selections (empty tiles in some splits), window-only rows
     and rows with no key at all."""
     n = [700, 300]

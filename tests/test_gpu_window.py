@@ -115,3 +115,15 @@ def test_attention_with_ring_window_peaky_and_sinks(orc, csa2):
     idx = np.stack([synth.distinct_indices(44 + i, n[i], 512) for i in range(2)])
     _attn_ring(orc, csa2, n, idx, newest=[513, 140], win_len=[128, 100], seed=59, qscale=6.0,
                sinks=synth.normal_f32(45, (64,)))
+
+
+def test_attention_with_ring_window_key_split_pairs(orc, csa2):
+    """64 queries: on 152 SMs each query takes a pair of CTAs, the first with the ring
+    window, the second adding the first one's partial to its own."""
+    n_q = 64
+    n = [600 + 7 * i for i in range(n_q)]
+    idx = np.stack([synth.distinct_indices(200 + i, n[i], 512) for i in range(n_q)])
+    idx[5, 200:] = -1
+    newest = [130 + 3 * i for i in range(n_q)]
+    win_len = [128 if i % 9 else 77 for i in range(n_q)]
+    _attn_ring(orc, csa2, n, idx, newest=newest, win_len=win_len, seed=60, sinks=synth.normal_f32(46, (64,)))
