@@ -25,9 +25,11 @@
 //             maxima raised (warp max reductions) and O^T and the running sums rescaled;
 //   O^T      += V^T P^T: 4 output chunks of 128 channels x 64 heads (TMEM cols 0..255)
 //             reading the same tile as an MN-major operand (K == V);
-//   epilogue O = O^T / l per head -> bf16 and lse; with S > 1 each CTA writes its raw
-//             partial and its (max, sum) per head to the workspace, one cluster barrier
-//             orders them, and each CTA of the cluster combines one slice of the heads.
+//   epilogue O = O^T / l per head -> bf16 and lse; with S > 1 the CTAs write their raw
+//             partials and (max, sum) per head to the workspace and one cluster barrier
+//             orders them: with S = 2 the second CTA adds the first one's partial to its
+//             own accumulator as it writes the output, with S > 2 each CTA of the
+//             cluster combines one slice of the heads.
 // Optional, from "From MLA to DSA to HCA/CSA": per-head attention sinks (a logit that
 // joins the softmax denominator and has no value; section "The sliding window") and
 // the partial RoPE of "What replaced MLA" (the queries' trailing 64 channels rotated

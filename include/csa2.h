@@ -205,8 +205,9 @@ const char* csa2_last_error(void);
 /* Workspace bytes needed by every call below for n_q queries of up to t_max visible
  * entries with heads_I indexer heads; scores_in_ws != 0 when the caller does not
  * provide a score array (the scores then live in the workspace).  For small batches
- * (n_q <= 76) it includes the attention's partial outputs: each query's key tiles are then
- * split over several CTAs whose fp32 partials a combine kernel merges (at most about 20 MB).
+ * (n_q < 76 on 152 SMs) it includes the attention's partial outputs: each query's key tiles
+ * are then split over a cluster of 2 to 5 CTAs that merge their fp32 partials through the
+ * workspace (n_q * S * 64 * 514 * 4 bytes for S CTAs per query, at most about 20 MB).
  * Bytes [0, 8) of the workspace are the error word (csa2_check); after a call that scores
  * (csa2_index_score, Full, Reindex) bytes [256, 256 + ceil(n_q / group) * (N * 64 + 1024))
  * hold the quantised indexer query, N = group * heads_I rows per group in the
