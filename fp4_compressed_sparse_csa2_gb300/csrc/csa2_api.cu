@@ -201,7 +201,8 @@ csa2_status run_pack(const void* latent, const void* idx_key, const int32_t* req
 
 csa2_status run_index(const csa2_cache& cache, const uint8_t* qpack, const float* w, int32_t heads_I, const int32_t* req,
                       const int32_t* n_visible, int64_t n_q, int32_t G, int64_t t_max, float* scores, int64_t ld,
-                      int32_t* err, cudaStream_t stream) {
+                      int32_t* err, cudaStream_t stream, bool early = false, const int32_t* new_req = nullptr,
+                      const int64_t* new_pos = nullptr, int64_t n_new = 0) {
   if (n_q == 0 || t_max == 0) return CSA2_OK;
   IndexArgs a{};
   a.idx_pages = cache.idx;
@@ -223,6 +224,12 @@ csa2_status run_index(const csa2_cache& cache, const uint8_t* qpack, const float
   a.stages = 16;
   a.tmem_cols = 512u;
   a.wait_ns = pipeline_wait_ns();
+  // early page copies: the previous kernel is this call's own pack kernel (see IndexArgs);
+  // the scan of the new entries stays short (decode-sized steps only)
+  a.early = early && n_new <= 256 ? 1 : 0;
+  a.new_req = new_req;
+  a.new_pos = new_pos;
+  a.n_new = a.early ? n_new : 0;
   const int64_t total = a.n_groups * a.tpg;
   const int64_t slots = static_cast<int64_t>(sm_count());  // one persistent CTA per SM
   const int grid = static_cast<int>(total < slots ? total : slots);
@@ -437,7 +444,7 @@ csa2_status run_step(const csa2_step* s, Mode mode, void* ws, size_t ws_bytes, c
                   s->q_idx, s->n_q, heads_I, s->group, base + L.qpack, err, stream);
     if (st != CSA2_OK) return st;
     st = run_index(s->cache, base + L.qpack, s->w, heads_I, s->req, s->n_visible, s->n_q, s->group, s->t_max, scores,
-                   ld, err, stream);
+                   ld, err, stream, true, s->new_req, s->new_pos, mode == kFull ? s->n_new : 0);
     if (st != CSA2_OK) return st;
     st = run_topk_cluster(scores, ld, s->n_visible, s->n_q, s->t_max, s->topk, s->topk_idx, err, stream);
     if (st != CSA2_OK) return st;
@@ -523,7 +530,8 @@ csa2_status csa2_index_score(const void* q_idx, const float* w, int32_t heads_I,
   st = run_pack(nullptr, nullptr, nullptr, nullptr, 0, *cache, q_idx, n_q, heads_I, group, base + L.qpack,
                 err_word(ws), s);
   if (st != CSA2_OK) return st;
-  return run_index(*cache, base + L.qpack, w, heads_I, req, n_visible, n_q, group, t_max, scores, ld, err_word(ws), s);
+  return run_index(*cache, base + L.qpack, w, heads_I, req, n_visible, n_q, group, t_max, scores, ld, err_word(ws), s,
+                   true);
 }
 
 csa2_status csa2_topk(const float* scores, int64_t ld, const int32_t* n_visible, int64_t n_q, int64_t t_max,

@@ -47,6 +47,15 @@ struct IndexArgs {
   uint32_t tmem_cols;
   int32_t* err;
   uint64_t wait_ns;  // bound of each pipeline wait (csa2_debug_set_wait_limit)
+  // early != 0: the previous kernel is this call's pack kernel, which starts the next
+  // kernel only after everything before it has completed and writes only the cache
+  // entries (new_req[i], new_pos[i]), i < n_new, and the packed queries; the producer may
+  // then copy the first pages of its range that hold none of those entries before
+  // griddepcontrol.wait
+  const int32_t* new_req;
+  const int64_t* new_pos;
+  int64_t n_new;
+  int32_t early;
 };
 
 struct TopkArgs {

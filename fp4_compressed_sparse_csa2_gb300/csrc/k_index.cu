@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
     tmem_relinquish();
   }
   pdl_trigger();
-  pdl_wait();  // the packed query groups and new cache entries come from the previous kernel
+  // griddepcontrol.wait (the packed query groups and the new cache entries come from the
+  // previous kernel) sits in each role: the producer may copy its first pages before it
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -181,28 +182,17 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
     uint32_t k = 0, ph = 0, n = 0, n_stages = 0, m = 0;
     bool ok = true;
     Segment sg;
-    for (int64_t g = g_first; ok && g <= g_last; ++g) {
-      if (!segment(a, g, begin, end, sg)) continue;
-      if (lane == 0) {
-        const uint32_t slot = m & 1u;
-        ok = mbar_wait(&q_empty[slot], ((m >> 1) & 1u) ^ 1u, abort, a.wait_ns);
-        if (ok) {
-          mbar_arrive_expect_tx(&q_full[slot], static_cast<uint32_t>(a.grp_bytes));
-          bulk_g2s(qslot + slot * kIdxPageBytes, a.qpack + g * a.grp_bytes, static_cast<uint32_t>(a.grp_bytes),
-                   &q_full[slot]);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      ++m;
-      for (int32_t t = sg.t0; t < sg.t1;) {
+    // Tiles [t, t_end) of segment sg into the ring (the copies of a stage of adjacent
+    // pages go as one bulk copy without a block table).
+    auto copy_tiles = [&](int32_t& t, int32_t t_end) {
+      while (t < t_end) {
         const uint32_t in_st = n % n_iss;
-        const int32_t left = sg.t1 - t;
+        const int32_t left = t_end - t;
         const int32_t cnt = left < static_cast<int32_t>(n_iss - in_st) ? left : static_cast<int32_t>(n_iss - in_st);
         if (in_st == 0) {
           if (lane == 0) ok = mbar_wait(&empty[k], ph ^ 1u, abort, a.wait_ns);
           ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
+          if (!ok) return;
         }
         uint8_t* dst = ring + (k * n_iss + in_st) * kPg;
         if (sg.bt_row == nullptr) {
@@ -237,7 +227,50 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
           }
         }
       }
+    };
+    // The first pages of the CTA's range go before griddepcontrol.wait (early), up to the
+    // ring's capacity and short of the first page holding an entry the pack kernel writes
+    // for the segment's request.  Only without a block table: a request's pages are then its
+    // own (page = request * max_pages + tile), so the pack kernel's writes are known by
+    // (request, tile) alone.
+    bool waited = false;
+    if (a.early == 0 || a.cache.block_table != nullptr) {
+      pdl_wait();
+      waited = true;
     }
+    for (int64_t g = g_first; ok && g <= g_last; ++g) {
+      if (!segment(a, g, begin, end, sg)) continue;
+      int32_t t = sg.t0;
+      if (!waited) {
+        int32_t first_new = sg.t1;  // first tile of this request written by the pack kernel
+        for (int64_t i = lane; i < a.n_new; i += 32)
+          if (__ldg(a.new_req + i) == sg.r) {
+            const int64_t tp = __ldg(a.new_pos + i) / kPage;
+            if (tp >= sg.t0 && tp < first_new) first_new = static_cast<int32_t>(tp);
+          }
+        first_new = __reduce_min_sync(0xffffffffu, first_new);
+        int32_t t_end = sg.t0 + static_cast<int32_t>(n_st * n_iss);
+        t_end = t_end < first_new ? t_end : first_new;
+        copy_tiles(t, t_end);
+        pdl_wait();
+        waited = true;
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        const uint32_t slot = m & 1u;
+        ok = mbar_wait(&q_empty[slot], ((m >> 1) & 1u) ^ 1u, abort, a.wait_ns);
+        if (ok) {
+          mbar_arrive_expect_tx(&q_full[slot], static_cast<uint32_t>(a.grp_bytes));
+          bulk_g2s(qslot + slot * kIdxPageBytes, a.qpack + g * a.grp_bytes, static_cast<uint32_t>(a.grp_bytes),
+                   &q_full[slot]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++m;
+      copy_tiles(t, sg.t1);
+    }
+    if (!waited) pdl_wait();  // no segment at all
     if (lane == 0) {
       // a partial last stage (also one left open when a wait ran out at a group boundary:
       // its copies are in flight) is closed, so that the drain below waits for it too
@@ -257,6 +290,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
   } else if (warp >= 1 && warp <= static_cast<int>(n_iss)) {
     if (lane == 0 && static_cast<uint32_t>(warp - 1) < n_iss) {
       // ------------------------------------------------------------ MMA issuers
+      pdl_wait();
       // issuer i takes the tiles n with n % n_iss == i: a single thread pays ~130 cycles per
       // dependent tcgen05 op, so the issuers (three, or two for N = 128) sit on different
       // warps to keep the tensor pipe and the copy ring moving
@@ -318,6 +352,7 @@ __global__ void __launch_bounds__(idx_threads(kSplit), 1) index_kernel(const Ind
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait();
     // thread = TMEM lane = key.  N <= 64: warpgroup wg takes the tiles with n % 3 == wg
     // and every column; N = 128: the tiles with n % 2 == wg % 2 and the 64 columns (the
     // query) wg / 2.

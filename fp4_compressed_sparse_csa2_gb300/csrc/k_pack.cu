@@ -33,8 +33,10 @@ __device__ __forceinline__ void load16(const __nv_bfloat16* src, float (&x)[16])
 // entry); items [n_new*40, +n_groups*128*8) pack indexer-query rows (rows >= N of a
 // group only clear their scale bytes).
 __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
-  pdl_trigger();
   pdl_wait();  // the previous step's kernels may still read the cache slots written here
+  // the next kernel (the indexer) starts only now: every kernel before this one has
+  // completed, so it may read the cache pages this kernel does not write before its wait
+  pdl_trigger();
   const int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t n_pack = a.n_new * 40;
   if (item < n_pack) {
