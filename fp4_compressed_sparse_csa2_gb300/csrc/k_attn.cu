@@ -618,7 +618,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
           tmem_ld32(tmem + lane_base + static_cast<uint32_t>(64 * hg + 32 * half), r);
           tmem_ld_wait();
         }
-#pragma unroll
         float p0[32];  // rank 0's partial for these heads (S == 2), all loads issued first
 #pragma unroll
         for (int i = 0; i < 32; ++i) p0[i] = S == 2 ? __ldcg(part0 + (32 * half + i) * CSA2_D + d) : 0.0f;
