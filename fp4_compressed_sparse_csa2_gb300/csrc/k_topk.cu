@@ -434,11 +434,6 @@ __device__ __forceinline__ uint32_t dsmem_map(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
 __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
   uint32_t old;
   asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
@@ -460,17 +455,6 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Warp-aggregated append to a counter in the leader's shared memory.
-__device__ __forceinline__ uint32_t dsmem_append(uint32_t counter, bool pred) {
-  const uint32_t m = __ballot_sync(0xffffffffu, pred);
-  if (m == 0) return 0;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(m) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = dsmem_atom_add(counter, static_cast<uint32_t>(__popc(m)));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  return base + __popc(m & ((1u << lane) - 1u));
-}
 
 // Sorts the k = 512 distinct indices in v (one per thread; padding INT_MAX) ascending
 // and writes the first k to out: each warp sorts its 32 with a shuffle network, then an
@@ -506,65 +490,6 @@ __device__ void sort_indices_out(int32_t v, int32_t* runs, int32_t* out, int k) 
   if (pos < k && v != INT_MAX) out[pos] = v;
 }
 
-// Writes the k distinct selected indices of [0, nv) in ascending order: a bitmap of the
-// row; warp w owns a contiguous run of words that its lanes read 32 consecutive words at
-// a time (no bank conflicts); a block prefix over the warps' popcounts, then a warp scan
-// per 32 words gives every set bit its rank.  bm: ceil(nv / 32) words of scratch.
-__device__ void bitmap_indices_out(const int32_t* sel, int k, int64_t nv, uint32_t* bm, uint32_t* s_warp,
-                                   int32_t* out) {
-  constexpr int kW = kTopkThreads / 32;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int W = static_cast<int>((nv + 31) >> 5);
-  const int per_w = (((W + kW - 1) / kW) + 31) & ~31;  // words per warp, a multiple of 32
-  for (int w = t; w < W; w += kTopkThreads) bm[w] = 0u;
-  __syncthreads();
-  for (int i = t; i < k; i += kTopkThreads) {
-    const int32_t v = sel[i];
-    atomicOr(&bm[v >> 5], 1u << (v & 31));
-  }
-  __syncthreads();
-  const int wb = warp * per_w;
-  uint32_t tot = 0;
-  for (int j = 0; j < per_w; j += 32) {
-    const int w = wb + j + lane;
-    tot += w < W ? static_cast<uint32_t>(__popc(bm[w])) : 0u;
-  }
-  tot = __reduce_add_sync(0xffffffffu, tot);
-  if (lane == 0) s_warp[warp] = tot;
-  __syncthreads();
-  if (warp == 0) {  // exclusive prefix over the warps
-    const uint32_t v0 = lane < kW ? s_warp[lane] : 0u;
-    uint32_t y = v0;
-#pragma unroll
-    for (int off = 1; off < kW; off <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, y, off);
-      if (lane >= off) y += v;
-    }
-    __syncwarp();
-    if (lane < kW) s_warp[kW + lane] = y - v0;
-  }
-  __syncthreads();
-  uint32_t run = s_warp[kW + warp];
-  for (int j = 0; j < per_w; j += 32) {
-    const int w = wb + j + lane;
-    uint32_t bits = w < W ? bm[w] : 0u;
-    const uint32_t c = static_cast<uint32_t>(__popc(bits));
-    uint32_t incl = c;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    uint32_t pos = run + incl - c;
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      if (pos < static_cast<uint32_t>(k)) out[pos] = w * 32 + b;
-      ++pos;
-      bits &= bits - 1u;
-    }
-    run += __shfl_sync(0xffffffffu, incl, 31);
-  }
-}
 
 // Exact selection among candidate (key, index) pairs that contain the `need` largest
 // keys: v* = the need-th largest key, found by radix selection on the key relative to
