@@ -99,6 +99,15 @@ __device__ __forceinline__ float lred_sum(const float* lred, int h) {
   return lred[h] + lred[64 + h] + lred[128 + h] + lred[192 + h];
 }
 
+// 2^x by the hardware approximation, denormal results flushed to zero: the softmax's P
+// values are rounded to f16 next, whose smallest subnormal (2^-24) lies far above the
+// flushed range, so P is the same as through exp2f.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Named barrier 1 over the CTA's 512 threads, and its OR-reduction form.
 __device__ __forceinline__ void cbar_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 __device__ __forceinline__ bool cbar_or(bool v) {
@@ -481,8 +490,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         uint32_t pk[8];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-          const float p0 = x[i] == -INFINITY ? 0.0f : exp2f(x[i] - ref_s[h0 + i]);
-          const float p1 = x[i + 1] == -INFINITY ? 0.0f : exp2f(x[i + 1] - ref_s[h0 + i + 1]);
+          const float p0 = x[i] == -INFINITY ? 0.0f : ex2_ftz(x[i] - ref_s[h0 + i]);
+          const float p1 = x[i + 1] == -INFINITY ? 0.0f : ex2_ftz(x[i + 1] - ref_s[h0 + i + 1]);
           const __half2 ph = __floats2half2_rn(p0, p1);
           const float2 pr = __half22float2(ph);
           lsum[i] += pr.x;
