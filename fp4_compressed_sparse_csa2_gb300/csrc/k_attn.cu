@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
       }
     }
   }
-  if (tid < kHeads) ref_s[tid] = -INFINITY;
+  if (tid < kHeads) ref_s[tid] = ml[tid] = -INFINITY;  // ml[0..63]: the vote's bound ref + 2^8 during the tiles
   tc_fence_before();
   __syncthreads();  // record ids, tile counts, converted queries (and the ring window)
   tc_fence_after();
@@ -457,10 +457,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         for (int i = 0; i < 16; ++i)
           x[i] = kv_ok ? (__uint_as_float(r[0][i]) + __uint_as_float(r[1][i])) * a.scale_log2 : -INFINITY;
       }
-      // the reference maxima live in shared memory (ref_s), read as broadcasts
+      // the reference maxima live in shared memory (ref_s, and ref + 2^8 in ml), read as
+      // broadcasts
       bool need = false, rescale = false;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) need |= x[i] > ref_s[h0 + i] + kRescaleThreshold;
+      for (int i = 0; i < 16; ++i) need |= x[i] > ml[h0 + i];
       if (cbar_or(need)) {
         // raise the reference maxima of the heads whose scores exceed them by 2^8
         float* tmax = reinterpret_cast<float*>(Ps);  // [4][64] scratch: P is rewritten below
@@ -478,6 +479,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
           const float al = nw == old ? 1.0f : (old == -INFINITY ? 0.0f : exp2f(old - nw));
           alpha[tid] = al;
           ref_s[tid] = nw;
+          ml[tid] = nw + kRescaleThreshold;
           ch = al != 1.0f;
         }
         rescale = cbar_or(ch) && o_started;  // alpha and ref_s are visible
@@ -490,8 +492,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnArgs a)
         uint32_t pk[8];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-          const float p0 = x[i] == -INFINITY ? 0.0f : ex2_ftz(x[i] - ref_s[h0 + i]);
-          const float p1 = x[i + 1] == -INFINITY ? 0.0f : ex2_ftz(x[i + 1] - ref_s[h0 + i + 1]);
+          // a masked key (x = -inf) gives 2^-inf = 0, also against a head whose reference
+          // is still -inf (the NaN of -inf - -inf is replaced by -inf)
+          const float p0 = ex2_ftz(fmaxf(x[i] - ref_s[h0 + i], -INFINITY));
+          const float p1 = ex2_ftz(fmaxf(x[i + 1] - ref_s[h0 + i + 1], -INFINITY));
           const __half2 ph = __floats2half2_rn(p0, p1);
           const float2 pr = __half22float2(ph);
           lsum[i] += pr.x;
